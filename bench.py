@@ -1,0 +1,363 @@
+"""Benchmark of the hybrid sliding-window two-pool decode path on GB300.
+
+One step = one decode step of the whole batch through the path: out-of-window
+SWA eviction (interval 128), alloc_decode in both pools + mapping, the
+per-batch SWA plan, then for every layer the KV store of the new token and
+paged attention (sliding layers through the SWA pool, full layers through
+req_to_token).  Inputs (q/k/v of the step, the KV cache built by a chunked
+prefill of the same method) are resident in HBM before timing; the KV read
+per step (~23 GB for the MiMo-shaped workload) is far larger than L2, so no
+flush is needed between steps.
+
+value  = algorithmic K+V bytes attended per step / device time per step (GB/s)
+e2e    = the same bytes / time per step when each step also copies its q/k/v
+         from pinned host memory and copies every layer's output back.
+roofline = the full-layer attention kernel alone (the dominant kernel), timed
+         with CUDA events around each of its launches.
+
+``--impl reference`` times the CPU oracle on a bounded sample of the same
+workload instead (single-threaded numpy, float64).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode KV GB/s (% HBM peak) and tokens/s; extend TFLOP/s; evict slots/s"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------- CPU oracle ---
+def cpu_sample(workload: str, budget_s: float):
+    """Times the oracle's attention on (request, full layer) pairs of the
+    workload's first decode step, until ``budget_s`` seconds of oracle time.
+    Runs in a child process with BLAS threads pinned to 1."""
+    code = f"""
+import json, time, sys
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+from hybrid_sliding_window_gb300 import synth
+from hybrid_sliding_window_gb300.workloads import SPECS, ESIZE, FULL
+from oracle import attention as A
+spec = SPECS[{workload!r}]
+seq = spec.seq_lens()
+es = ESIZE[spec.dtype]
+t_or = 0.0; nbytes = 0; pairs = 0
+full_layers = [l for l, (k, w, h) in enumerate(spec.layers) if k == FULL]
+b = 0
+while t_or < {budget_s} and pairs < 4096:
+    l = full_layers[pairs % len(full_layers)]
+    kind, w, hkv = spec.layers[l]
+    p = int(seq[b % spec.batch]) - 1
+    J = np.arange(0, p + 1)
+    row = (b % spec.batch) + 1
+    K = synth.tokens(spec.seed, synth.STREAM_K, l, np.full(len(J), row), J, hkv, spec.D)
+    V = synth.tokens(spec.seed, synth.STREAM_V, l, np.full(len(J), row), J, hkv, spec.D)
+    q = synth.tokens(spec.seed, synth.STREAM_Q, l, [row], [p], spec.Hq, spec.D)[0]
+    sinks = synth.sinks(spec.seed, l, spec.Hq) if spec.sinks else None
+    t0 = time.perf_counter()
+    A.attend_heads(q, K, V, sinks, 1.0 / np.sqrt(spec.D))
+    t_or += time.perf_counter() - t0
+    nbytes += len(J) * hkv * spec.D * 2 * es
+    pairs += 1
+    b += 1
+print(json.dumps(dict(seconds=t_or, bytes=nbytes, pairs=pairs)))
+"""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=600)
+    if r.returncode != 0:
+        raise RuntimeError("cpu sample failed: " + r.stderr[-2000:])
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": round(d["bytes"] / d["seconds"] / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{d['pairs']} (request, full layer) attention problems of the first decode "
+                      f"step, all {SPECS_HQ(workload)} query heads each, {d['bytes'] / 1e9:.2f} GB of "
+                      f"K+V in {d['seconds']:.1f} s of float64 numpy on one host core"}
+
+
+def SPECS_HQ(workload):
+    from hybrid_sliding_window_gb300.workloads import SPECS
+    return SPECS[workload].Hq
+
+
+# ------------------------------------------------------------------ clocks ---
+class ClockSampler:
+    def __init__(self, index=0):
+        self.proc = None
+        self.path = None
+        self.index = index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader",
+                                          "-lms", "200", "-i", str(self.index)],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        def mhz(s):
+            try:
+                return float(s.split()[0])
+            except Exception:
+                return None
+        sm = [mhz(r[1]) for r in rows if mhz(r[1]) is not None]
+        mx = [mhz(r[2]) for r in rows if mhz(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- native ---
+def run_native(args, rank, world):
+    import numpy as np
+    import torch
+    from hybrid_sliding_window_gb300 import api
+    from hybrid_sliding_window_gb300.workloads import SPECS, DecodeState, FULL
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    api.lib()
+    spec = SPECS[args.workload]
+    W, K = args.warmup, args.steps
+    st = DecodeState(spec, max_steps=W + 2 * K + 4)
+    t0 = time.time()
+    st.prefill()
+    setup_s = time.time() - t0
+    st.alloc_decode_buffers()
+    inputs = st.make_decode_inputs(W + 2 * K)
+    torch.cuda.synchronize()
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+
+    def barrier():
+        if dist:
+            tdist.barrier()
+        torch.cuda.synchronize()
+
+    for s in range(W):
+        st.decode_step(inputs[s])
+    full_layers = [l for l, (k, _, _) in enumerate(spec.layers) if k == FULL]
+    ev = {l: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)] for l in full_layers}
+    bytes_steps = []
+    attn_bytes = []
+    barrier()
+    clk = ClockSampler(local)
+    clk.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(K):
+        inp = inputs[W + s]
+        b = st.kv_bytes_per_step(inp["seq_h"])
+        bytes_steps.append(b["total"])
+        attn_bytes.append(b["full"] / len(full_layers))
+        st.decode_step(inp, {l: ev[l][s] for l in full_layers})
+    e1.record()
+    barrier()
+    clocks = clk.stop()
+    t_ms = e0.elapsed_time(e1)
+    durs = [ev[l][s][0].elapsed_time(ev[l][s][1]) for l in full_layers for s in range(K)]
+    full_attn_ms = sum(durs) / len(durs)
+    assert api.swa_device_check(st.ctx) == 0, "device-side check flagged an error"
+
+    # e2e: the same steps fed from pinned host memory, outputs copied back.
+    host_in = []
+    for s in range(K):
+        inp = inputs[W + K + s]
+        host_in.append({key: [t.cpu().pin_memory() for t in inp[key]] for key in ("q", "k", "v")})
+    dev_in = {key: [torch.empty_like(t) for t in inputs[0][key]] for key in ("q", "k", "v")}
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in st.outs]
+    h2d = sum(t.numel() * t.element_size() for key in ("q", "k", "v") for t in dev_in[key])
+    d2h = sum(o.numel() * o.element_size() for o in st.outs)
+    e2e_bytes = 0
+    barrier()
+    x0 = torch.cuda.Event(enable_timing=True)
+    x1 = torch.cuda.Event(enable_timing=True)
+    x0.record()
+    for s in range(K):
+        src = inputs[W + K + s]
+        for key in ("q", "k", "v"):
+            for d_, h_ in zip(dev_in[key], host_in[s][key]):
+                d_.copy_(h_, non_blocking=True)
+        step_inp = dict(src, q=dev_in["q"], k=dev_in["k"], v=dev_in["v"])
+        e2e_bytes += st.kv_bytes_per_step(src["seq_h"])["total"]
+        st.decode_step(step_inp)
+        for h_, o in zip(host_out, st.outs):
+            h_.copy_(o, non_blocking=True)
+    x1.record()
+    barrier()
+    e2e_ms = x0.elapsed_time(x1)
+    assert api.swa_device_check(st.ctx) == 0
+
+    t_ms_max = t_ms
+    e2e_max = e2e_ms
+    tot_bytes = sum(bytes_steps)
+    tot_e2e = e2e_bytes
+    if dist:
+        tt = torch.tensor([t_ms, e2e_ms], dtype=torch.float64, device="cuda")
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+        t_ms_max, e2e_max = tt.tolist()
+        bb = torch.tensor([float(tot_bytes), float(tot_e2e)], dtype=torch.float64, device="cuda")
+        tdist.all_reduce(bb, op=tdist.ReduceOp.SUM)
+        tot_bytes, tot_e2e = bb.tolist()
+    if rank != 0:
+        return None
+    peak, peak_kind = peaks()
+    value = tot_bytes / (t_ms_max / 1e3) / 1e9
+    ach = (sum(attn_bytes) / len(attn_bytes)) / (full_attn_ms / 1e3) / 1e9
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", f"{args.workload}_decode_traffic.json")
+    if os.path.exists(tp):
+        try:
+            with open(tp) as f:
+                tj = json.load(f)
+            if tj.get("kernel_source_hash") == kernel_hash():
+                traffic = tj["bytes_per_launch"]
+        except Exception:
+            traffic = None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(t_ms_max / K, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
+        "data": "synthetic",
+        "config": {"workload": spec.description, "batch_per_gpu": spec.batch,
+                   "kv_bytes_per_step": int(sum(bytes_steps) / K),
+                   "l2": "no flush: each step reads far more KV than the 129 MB L2",
+                   "pools_tokens": {"full": st.size_full, "swa": st.size_swa},
+                   "setup_s": round(setup_s, 1)},
+        "hbm_frac": round(value / peak, 4),
+        "tokens_per_s": round(spec.batch * world * K / (t_ms_max / 1e3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(ach / peak, 4), "traffic": traffic,
+                     "kernel": "swa_attn_decode on full layers",
+                     "peak_source": peak_kind, "avg_launch_ms": round(full_attn_ms, 4)},
+        "e2e": {"value": round(tot_e2e / (e2e_max / 1e3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clocks,
+        "gpu_launches": st.launches_per_step() * K,
+        "attn_path": api.swa_last_attn_path(st.ctx),
+    }
+    if world == 1 and not args.no_cpu:
+        try:
+            line["cpu_baseline"] = cpu_sample(args.workload, args.cpu_seconds)
+        except Exception as e:  # the GPU number stands; say why the baseline is missing
+            line["cpu_baseline"] = {"error": str(e)[:300]}
+    return line
+
+
+def kernel_hash():
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "hybrid_sliding_window_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".h")):
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------- reference ---
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    K, W = args.steps, args.warmup
+    per = max(2.0, min(20.0, 120.0 / max(1, K + W)))
+    vals = []
+    sample = None
+    for i in range(W + K):
+        r = cpu_sample(args.workload, per)
+        if i >= W:
+            vals.append(r["value"])
+            sample = r["sample"]
+    v = statistics.mean(vals)
+    from hybrid_sliding_window_gb300.workloads import SPECS
+    spec = SPECS[args.workload]
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": spec.description},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="mimo", choices=["mimo", "gptoss", "llama4"])
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and args.impl == "native":
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_native(args, rank, world)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl == "native":
+        import torch.distributed as tdist
+        tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

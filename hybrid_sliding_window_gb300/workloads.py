@@ -1,0 +1,320 @@
+"""Seeded synthetic workloads shaped like the pages' hybrid models, and a GPU
+decode state that builds its KV cache by replaying the method itself.
+
+Model shapes ("SWA in SGLang" design note, "design"): MiMo-V2-Flash (48
+layers, 39 sliding with window 128 and 8 KV heads, 9 full with 4 KV heads),
+GPT-OSS (sliding and full layers alternating), Llama4 (3 of every 4 layers
+chunked-local, the 4th global).  The pages do not give MiMo's
+hybrid_layer_pattern; full layers sit at every 5th position from layer 4.
+
+Everything here calls the C library through ``api``; inputs (q, k, v,
+sinks) come from ``synth``.  The state keeps a trace of the allocation /
+eviction calls it made so that a test can replay the same sequence on the
+CPU oracle.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+from . import api, synth
+
+FULL, SLIDING, CHUNKED = api.LAYER_FULL, api.LAYER_SLIDING, api.LAYER_CHUNKED
+DTYPES = {"f32": api.DTYPE_F32, "bf16": api.DTYPE_BF16, "e4m3": api.DTYPE_E4M3}
+ESIZE = {"f32": 4, "bf16": 2, "e4m3": 1}
+
+
+def mimo_layers():
+    return [(FULL, 0, 4) if l % 5 == 4 else (SLIDING, 127, 8) for l in range(48)]
+
+
+def gptoss_layers():
+    return [(SLIDING, 127, 8) if l % 2 == 0 else (FULL, 0, 8) for l in range(24)]
+
+
+def llama4_layers(groups=12):
+    return [(FULL, 0, 8) if l % 4 == 3 else (CHUNKED, 8192, 8) for l in range(4 * groups)]
+
+
+@dataclasses.dataclass
+class Spec:
+    name: str
+    layers: list
+    Hq: int
+    D: int
+    dtype: str
+    ps: int
+    batch: int
+    seq_kind: str            # "uniform", "loguniform", "fixed"
+    seq_lo: int
+    seq_hi: int
+    r: float
+    interval: int
+    seed: int
+    layout: str = "per_layer"
+    sinks: bool = True
+    chunk: int = 8192
+    description: str = ""
+
+    def seq_lens(self) -> np.ndarray:
+        if self.seq_kind == "uniform":
+            return synth.seq_lens_uniform(self.seed, self.batch, self.seq_lo, self.seq_hi)
+        if self.seq_kind == "loguniform":
+            return synth.seq_lens_log_uniform(self.seed, self.batch, self.seq_lo, self.seq_hi)
+        return np.full(self.batch, self.seq_lo, dtype=np.int64)
+
+    def lookback(self) -> int:
+        lb = 0
+        for kind, w, _ in self.layers:
+            if kind == SLIDING:
+                lb = max(lb, w)
+            elif kind == CHUNKED:
+                lb = max(lb, w - 1)
+        return lb
+
+
+SPECS = {
+    "mimo": Spec("mimo", mimo_layers(), 64, 128, "bf16", 64, 64, "uniform", 4096, 32768, 0.8,
+                 128, 1, description="MiMo-V2-Flash-shaped decode: 48 layers (39 sliding W=128 "
+                 "with 8 KV heads, 9 full with 4 KV heads), 64 query heads, D=128, bf16 KV, "
+                 "page 64, B=64, seqlens U[4096,32768], r=0.8, eviction interval 128"),
+    "gptoss": Spec("gptoss", gptoss_layers(), 64, 64, "bf16", 16, 128, "loguniform", 1024, 16384,
+                   0.8, 128, 2, description="GPT-OSS-shaped decode: 24 layers alternating "
+                   "sliding (W=128) and full, 64 query heads, 8 KV heads, D=64, bf16 KV, page 16, "
+                   "B=128, seqlens log-uniform [1024,16384], r=0.8"),
+    "llama4": Spec("llama4", llama4_layers(), 40, 128, "e4m3", 64, 16, "fixed", 131072, 131072,
+                   0.05, 128, 4, layout="envelope", sinks=False, description="Llama4-shaped "
+                   "long-context decode: 12 x [3 chunked-local (C=8192) + 1 global] layers, 40 "
+                   "query heads, 8 KV heads, D=128, FP8-E4M3 KV in the page-major envelope, page 64, "
+                   "B=16 at seqlen 131072, r=0.05"),
+}
+
+
+def sizing(spec: Spec, seq: np.ndarray, headroom: int):
+    """Pool sizes by the pages' rule: cell = F*L_full + r*S*L_swa, with the
+    memory budget chosen as cell * N_full for the full-pool need, raised if
+    the SWA pool would not hold the prefill's live window."""
+    ps = spec.ps
+    es = ESIZE[spec.dtype]
+    full_h = [h for k, _, h in spec.layers if k == FULL]
+    swa_h = [h for k, _, h in spec.layers if k != FULL]
+    F = (full_h[0] if full_h else 0) * 2 * spec.D * es
+    S = (swa_h[0] if swa_h else 0) * 2 * spec.D * es
+    Lf, Ls = len(full_h), len(swa_h)
+    n_full = int(sum(math.ceil((int(s) + headroom) / ps) * ps + ps for s in seq))
+    lb = spec.lookback()
+    # Live SWA slots at the prefill peak (one request group at a time).
+    swa_min = spec.batch * (lb + spec.interval + 3 * ps) + spec.chunk + lb + 2 * ps
+    n_full = max(n_full, int(math.ceil(swa_min / spec.r)))
+    cell = F * Lf + spec.r * S * Ls
+    M = int(math.ceil(cell * (n_full + ps)))
+    nf, ns = api.swa_pool_sizes(M, F, S, Lf, Ls, spec.r, ps, lb)
+    return nf, ns, M
+
+
+class DecodeState:
+    """A whole decode workload resident on one GPU."""
+
+    def __init__(self, spec: Spec, max_steps: int = 64, device: str = "cuda", trace: bool = False,
+                 poison_page0: bool = False):
+        self.spec = spec
+        self.dev = device
+        self.seq0 = spec.seq_lens()
+        self.B = spec.batch
+        self.max_steps = max_steps
+        self.ps = spec.ps
+        nf, ns, M = sizing(spec, self.seq0, max_steps + spec.interval)
+        self.size_full, self.size_swa, self.mem_budget = nf, ns, M
+        self.max_ctx = int(self.seq0.max()) + max_steps + 2 * spec.ps
+        self.max_seq_len = int(self.seq0.max()) + max_steps
+        self.trace = [] if trace else None
+        st = api._STORE_TORCH[DTYPES[spec.dtype]]
+        gl = []
+        self.kv = []
+        self.full_env = self.swa_env = None
+        if spec.layout == "per_layer":
+            for kind, w, hkv in spec.layers:
+                n = (nf if kind == FULL else ns) + spec.ps
+                k = torch.empty((n, hkv, spec.D), dtype=st, device=device)
+                v = torch.empty((n, hkv, spec.D), dtype=st, device=device)
+                if poison_page0:
+                    k[:spec.ps].fill_(float("nan")) if st != torch.uint8 else k[:spec.ps].fill_(0x7F)
+                    v[:spec.ps].fill_(float("nan")) if st != torch.uint8 else v[:spec.ps].fill_(0x7F)
+                self.kv.append((k, v))
+                gl.append(dict(kind=kind, window=w, num_kv_heads=hkv, k=k, v=v))
+        else:
+            lf = sum(1 for k, _, _ in spec.layers if k == FULL)
+            ls = len(spec.layers) - lf
+            hf = [h for k, _, h in spec.layers if k == FULL][0]
+            hs = [h for k, _, h in spec.layers if k != FULL][0]
+            rb_f = hf * spec.D * ESIZE[spec.dtype]
+            rb_s = hs * spec.D * ESIZE[spec.dtype]
+            self.full_env = torch.empty(((nf // spec.ps + 2) * 2 * lf * spec.ps) * rb_f,
+                                        dtype=torch.uint8, device=device)
+            self.swa_env = torch.empty(((ns // spec.ps + 2) * 2 * ls * spec.ps) * rb_s,
+                                       dtype=torch.uint8, device=device)
+            if poison_page0:
+                self.full_env[: 2 * lf * spec.ps * rb_f].fill_(0x7F)
+                self.swa_env[: 2 * ls * spec.ps * rb_s].fill_(0x7F)
+            for kind, w, hkv in spec.layers:
+                gl.append(dict(kind=kind, window=w, num_kv_heads=hkv))
+        self.ctx = api.SwaCtx(gl, spec.ps, nf, ns, spec.Hq, spec.D, DTYPES[spec.dtype],
+                              api.LAYOUT_PER_LAYER if spec.layout == "per_layer"
+                              else api.LAYOUT_ENVELOPE, False, max(self.B, 1),
+                              self.full_env, self.swa_env, device=device)
+        self.rt = torch.zeros((self.B + 1, self.max_ctx), dtype=torch.int32, device=device)
+        self.rows = np.arange(1, self.B + 1, dtype=np.int64)
+        self.rows_d = torch.tensor(self.rows, device=device)
+        self.lens = np.zeros(self.B, np.int64)        # tokens with stored KV
+        self.evicted = np.zeros(self.B, np.int64)
+        self.evicted_d = torch.zeros(self.B, dtype=torch.int64, device=device)
+        self.sinks_h = [synth.sinks(spec.seed, l, spec.Hq) if spec.sinks else None
+                        for l in range(len(spec.layers))]
+        self.sinks_d = [torch.tensor(s, device=device) if s is not None else None for s in self.sinks_h]
+        self.scale = 1.0 / math.sqrt(spec.D)
+        self.in_dtype = torch.float32 if spec.dtype == "f32" else torch.bfloat16
+        self.stream = torch.cuda.current_stream()
+
+    # -- helpers ------------------------------------------------------------
+    def _synth(self, stream_id, layer, req_d, pos_d, heads):
+        out = torch.empty((req_d.numel(), heads, self.spec.D), dtype=self.in_dtype, device=self.dev)
+        api.swa_synth_tokens(self.spec.seed, stream_id, layer, req_d, pos_d, heads, self.spec.D, out)
+        return out
+
+    def _evict(self, idx, interval):
+        """Eviction pass over batch entries idx (numpy)."""
+        idx_d = torch.tensor(idx, device=self.dev)
+        ev_h = self.evicted[idx].copy()
+        ev_d = self.evicted_d[idx_d].contiguous()
+        pre = self.lens[idx].copy()
+        if self.trace is not None:
+            self.trace.append(("evict", self.rows[idx].tolist(), pre.tolist(), ev_h.tolist(), interval))
+        api.swa_evict_swa(self.ctx, self.rt, self.rows_d[idx_d].contiguous(),
+                          torch.tensor(pre, device=self.dev), ev_d, pre, ev_h, interval=interval)
+        self.evicted[idx] = ev_h
+        self.evicted_d[idx_d] = ev_d
+
+    def _extend(self, idx, new_lens):
+        """alloc_extend + store of positions lens..new_lens-1 for entries idx."""
+        pre = self.lens[idx].copy()
+        seq = np.asarray(new_lens, np.int64)
+        n = int((seq - pre).sum())
+        if self.trace is not None:
+            self.trace.append(("extend", self.rows[idx].tolist(), pre.tolist(), seq.tolist()))
+        out_f = torch.empty(n, dtype=torch.int64, device=self.dev)
+        out_s = torch.empty(n, dtype=torch.int64, device=self.dev)
+        idx_d = torch.tensor(idx, device=self.dev)
+        api.swa_alloc_extend(self.ctx, torch.tensor(pre, device=self.dev),
+                             torch.tensor(seq, device=self.dev), None, pre, seq, out_f, out_s,
+                             req_to_token=self.rt, req_idx=self.rows_d[idx_d].contiguous())
+        reqs = torch.tensor(np.repeat(self.rows[idx], seq - pre), device=self.dev)
+        pos = torch.tensor(np.concatenate([np.arange(p, s) for p, s in zip(pre, seq)]),
+                           device=self.dev)
+        for l, (kind, w, hkv) in enumerate(self.spec.layers):
+            k = self._synth(synth.STREAM_K, l, reqs, pos, hkv)
+            v = self._synth(synth.STREAM_V, l, reqs, pos, hkv)
+            api.swa_store_kv(self.ctx, l, k, v, out_f, out_s)
+        self.lens[idx] = seq
+
+    def prefill(self, prompt=None):
+        """Chunked prefill of every request to ``prompt`` (default seq - 1)
+        tokens, evicting out-of-window SWA KV before each chunk; requests
+        are admitted in groups the SWA pool can hold."""
+        spec = self.spec
+        prompt = self.seq0 - 1 if prompt is None else np.asarray(prompt, np.int64)
+        per_req = spec.chunk + spec.lookback() + 2 * spec.ps
+        rest = spec.lookback() + 2 * spec.ps
+        g = max(1, min(self.B, (self.size_swa - self.B * rest) // per_req))
+        for g0 in range(0, self.B, g):
+            grp = np.arange(g0, min(self.B, g0 + g))
+            while (self.lens[grp] < prompt[grp]).any():
+                sel = grp[self.lens[grp] < prompt[grp]]
+                self._evict(sel, 0)
+                self._extend(sel, np.minimum(self.lens[sel] + spec.chunk, prompt[sel]))
+        torch.cuda.synchronize()
+
+    # -- decode -----------------------------------------------------------------
+    def make_decode_inputs(self, n_steps: int):
+        """q/k/v of n_steps decode steps for every layer, drawn on the device."""
+        spec = self.spec
+        steps = []
+        for s in range(n_steps):
+            pos = torch.tensor(self.lens + s, device=self.dev)   # position of the new token
+            reqs = self.rows_d
+            q, k, v = [], [], []
+            for l, (kind, w, hkv) in enumerate(spec.layers):
+                q.append(self._synth(synth.STREAM_Q, l, reqs, pos, spec.Hq))
+                k.append(self._synth(synth.STREAM_K, l, reqs, pos, hkv))
+                v.append(self._synth(synth.STREAM_V, l, reqs, pos, hkv))
+            seq_h = self.lens + s + 1
+            steps.append(dict(q=q, k=k, v=v, seq_h=seq_h, pre_h=seq_h - 1,
+                              seq_d=torch.tensor(seq_h, device=self.dev),
+                              pre_d=torch.tensor(seq_h - 1, device=self.dev)))
+        return steps
+
+    def alloc_decode_buffers(self):
+        spec = self.spec
+        self.out_full = torch.empty(self.B, dtype=torch.int64, device=self.dev)
+        self.out_swa = torch.empty(self.B, dtype=torch.int64, device=self.dev)
+        self.plan = torch.zeros(api.swa_plan_bytes(self.ctx, self.B, 1), dtype=torch.uint8,
+                                device=self.dev)
+        wsb = max(api.swa_attn_decode_ws_bytes(self.ctx, l, self.B, self.max_seq_len)
+                  for l in range(len(spec.layers)))
+        self.ws = torch.zeros(wsb, dtype=torch.uint8, device=self.dev)
+        self.outs = [torch.empty((self.B, spec.Hq, spec.D), dtype=self.in_dtype, device=self.dev)
+                     for _ in spec.layers]
+
+    def decode_step(self, inp, attn_events=None):
+        """One decode step: evict (interval), alloc_decode, plan, then per layer
+        store_kv + attn_decode.  attn_events: optional dict layer -> (start,
+        end) CUDA events recorded around that layer's attention launch."""
+        spec = self.spec
+        if self.trace is not None:
+            self.trace.append(("evict", self.rows.tolist(), inp["pre_h"].tolist(),
+                               self.evicted.tolist(), spec.interval))
+        api.swa_evict_swa(self.ctx, self.rt, self.rows_d, inp["pre_d"], self.evicted_d,
+                          inp["pre_h"], self.evicted, interval=spec.interval)
+        if self.trace is not None:
+            self.trace.append(("decode", self.rows.tolist(), inp["seq_h"].tolist()))
+        api.swa_alloc_decode(self.ctx, inp["seq_d"], None, inp["seq_h"], self.out_full,
+                             self.out_swa, req_to_token=self.rt, req_idx=self.rows_d)
+        api.swa_plan(self.ctx, self.rt, self.rows_d, None, inp["seq_d"], self.plan, 1)
+        for l in range(len(spec.layers)):
+            api.swa_store_kv(self.ctx, l, inp["k"][l], inp["v"][l], self.out_full, self.out_swa)
+            ev = attn_events.get(l) if attn_events else None
+            if ev is not None:
+                ev[0].record()
+            api.swa_attn_decode(self.ctx, l, self.rt, self.rows_d, inp["seq_d"], self.max_seq_len,
+                                self.plan, inp["q"][l], self.sinks_d[l], self.scale, self.outs[l],
+                                self.ws)
+            if ev is not None:
+                ev[1].record()
+        self.lens = inp["seq_h"].copy()
+
+    def launches_per_step(self) -> int:
+        # evict (3) + alloc_decode (2) + plan (1) + per layer store (1) + attention (1)
+        return 3 + 2 + 1 + 2 * len(self.spec.layers)
+
+    def kv_bytes_per_step(self, seq_h=None) -> dict:
+        """Algorithmic K+V bytes read by attention in one decode step."""
+        spec = self.spec
+        seq = self.lens + 1 if seq_h is None else seq_h
+        es = ESIZE[spec.dtype]
+        full = swa = 0
+        for kind, w, hkv in spec.layers:
+            p = seq - 1
+            if kind == FULL:
+                n = seq
+            elif kind == SLIDING:
+                n = p - np.maximum(0, p - w) + 1
+            else:
+                n = p - (p // w) * w + 1
+            b = int(n.sum()) * hkv * spec.D * 2 * es
+            if kind == FULL:
+                full += b
+            else:
+                swa += b
+        return {"full": full, "swa": swa, "total": full + swa}

@@ -1,0 +1,347 @@
+/*
+ * libswa - hybrid sliding-window (SWA) two-pool KV cache and paged attention
+ * for one NVIDIA GB300 (sm_103a).
+ *
+ * Method (source pages, cited by title and section):
+ *   [SWA note]  "SWA in SGLang" design note (zdszero.github.io/swa.html)
+ *   [Pools 15]  "SGLang source teardown (15): memory pools and allocators"
+ *   [PR 34602]  SGLang PR #34602 summary, "unified pool MHA/SWA -> dense
+ *               per-layer views" (prhub.com.cn)
+ *
+ * One token has two addresses: a slot in the FULL pool (its primary
+ * address, kept while the request lives) and, through the mapping
+ * full_to_swa[full_slot], a slot in the SWA pool that is returned once the
+ * token slides out of every sliding window ([SWA note], "abstraction: one
+ * token, two addresses").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Ownership: the caller allocates and owns every device buffer (KV pools,
+ *   the state blob, req_to_token, q/out, plan and workspaces).  The library
+ *   allocates no device memory; it keeps host-side mirrors of the free
+ *   counts only.
+ * - Asynchrony: every call enqueues work on `stream` and returns without
+ *   synchronising, except swa_device_check() and swa_sync_counts().  Host
+ *   copies of lengths are passed next to device copies so capacity checks
+ *   need no device read ([Pools 15], "alloc_decode": the CPU copy of the
+ *   lengths avoids an implicit sync).
+ * - Errors: a non-SWA_OK status leaves device state and host mirrors
+ *   untouched unless stated; swa_last_error() gives a message.  Kernels never
+ *   trap: device-side checks (a read of mapping value 0 inside a window, a
+ *   page count that disagrees with the host's) set an error word that
+ *   swa_device_check() reads.
+ * - Index types: slots, lengths, the mapping and free lists are int64;
+ *   req_to_token is int32 ([Pools 15], ReqToTokenPool).  Slot 0 / page 0 of
+ *   every pool is the padding sink and is never handed out.
+ * - Layouts of one KV row (one token, one layer): [Hkv][D] elements.
+ *   PER_LAYER: K and V of layer l are separate arrays of
+ *   (pool_size + page_size) rows ([Pools 15], "second mapping", MHA pool).
+ *   ENVELOPE: one byte buffer per pool of page envelopes
+ *   [L0_K*ps | L0_V*ps | L1_K*ps | ...]; the row of slot t of pool-layer l is
+ *   kernel_id(t) + (2l or 2l+1)*ps with kernel_id(t) = (t/ps)*(ps*2L) + t%ps
+ *   ([PR 34602], "implementation", step 1).
+ * - Streams: swa_stream_t is a cudaStream_t (0 = legacy default stream).
+ */
+#ifndef SWA_H
+#define SWA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *swa_stream_t;
+typedef struct swa_ctx swa_ctx;
+
+typedef enum swa_status {
+  SWA_OK = 0,
+  SWA_ERR_NOMEM = 1,        /* not enough free pages; nothing was changed      */
+  SWA_ERR_INVALID = 2,      /* bad argument (null pointer, size, layer, ...)   */
+  SWA_ERR_CONFIG = 3,       /* configuration rejected at create time           */
+  SWA_ERR_CUDA = 4,         /* a CUDA runtime call failed                      */
+  SWA_ERR_DEVICE_CHECK = 5  /* a kernel's own check failed (swa_device_check)  */
+} swa_status;
+
+enum swa_layer_kind {
+  SWA_LAYER_FULL = 0,     /* keys 0..p, full pool                               */
+  SWA_LAYER_SLIDING = 1,  /* keys max(0,p-window)..p, SWA pool; window excludes
+                             the current token ([SWA note], "which models,
+                             which layers": sliding_window - 1)               */
+  SWA_LAYER_CHUNKED = 2   /* keys floor(p/C)*C..p with C = window, SWA pool    */
+};
+
+enum swa_dtype { SWA_DTYPE_F32 = 0, SWA_DTYPE_BF16 = 1, SWA_DTYPE_E4M3 = 2 };
+enum swa_layout { SWA_LAYOUT_PER_LAYER = 0, SWA_LAYOUT_ENVELOPE = 1 };
+
+/* Error-word bits set by device-side checks. */
+enum swa_device_error {
+  SWA_DEVERR_WINDOW_EVICTED = 1,  /* an attended key's SWA mapping was 0        */
+  SWA_DEVERR_COUNT = 2,           /* freed page count differs from host count  */
+  SWA_DEVERR_RANGE = 4,           /* slot / page / position out of range       */
+  SWA_DEVERR_SORT_CAP = 8         /* an eviction range exceeded the sort size  */
+};
+
+typedef struct swa_layer {
+  int32_t kind;          /* enum swa_layer_kind                                 */
+  int32_t window;        /* SLIDING: exclusive window Wx; CHUNKED: chunk C      */
+  int32_t num_kv_heads;  /* Hkv of this layer (GQA: Hq % Hkv == 0)              */
+  int32_t reserved;
+  void *k;               /* PER_LAYER: K rows [pool_size + page_size][Hkv][D]   */
+  void *v;               /* PER_LAYER: V rows, same shape; ENVELOPE: unused     */
+} swa_layer;
+
+typedef struct swa_config {
+  int32_t num_layers;
+  int32_t page_size;      /* ps >= 1                                              */
+  int64_t size_full;      /* full pool token capacity, multiple of ps             */
+  int64_t size_swa;       /* SWA pool token capacity, multiple of ps              */
+  int32_t num_q_heads;    /* Hq                                                   */
+  int32_t head_dim;       /* D (K and V), multiple of 8, <= 256                   */
+  int32_t kv_dtype;       /* enum swa_dtype of the stored KV                      */
+  int32_t layout;         /* enum swa_layout                                      */
+  int32_t need_sort;      /* 1: stage released pages, sort-merge when short       */
+  int32_t max_batch;      /* largest bs of any call                               */
+  const swa_layer *layers;/* num_layers entries, copied at create                 */
+  void *full_envelope;    /* ENVELOPE: full-pool byte buffer                      */
+  int64_t full_envelope_bytes;
+  void *swa_envelope;     /* ENVELOPE: SWA-pool byte buffer                       */
+  int64_t swa_envelope_bytes;
+} swa_config;
+
+/* Device pointers into the state blob, for inspection by tests. */
+typedef struct swa_state_view {
+  int64_t *mapping;        /* size_full + ps + 1 entries, last = -1           */
+  int64_t *free_full;      /* ring of num_pages_full page ids                 */
+  int64_t *staged_full;    /* num_pages_full                                  */
+  int64_t *free_swa;       /* ring of num_pages_swa page ids                  */
+  int64_t *staged_swa;
+  int64_t *counters;       /* see SWA_CTR_* below                             */
+  int64_t num_pages_full;
+  int64_t num_pages_swa;
+} swa_state_view;
+
+enum swa_counter {
+  SWA_CTR_FULL_HEAD = 0, SWA_CTR_FULL_COUNT = 1, SWA_CTR_FULL_STAGED = 2,
+  SWA_CTR_SWA_HEAD = 3, SWA_CTR_SWA_COUNT = 4, SWA_CTR_SWA_STAGED = 5,
+  SWA_CTR_ERROR = 6
+};
+
+/* ---------------------------------------------------------------- sizing --
+ * Two-pool sizing ([SWA note], "how memory is split:
+ * --swa-full-tokens-ratio"): cell = F*L_full + r*S*L_swa,
+ * N_full = floor(M / cell), N_swa = r*N_full, both aligned down to a page.
+ * F, S: KV bytes of one token in one full / SWA layer
+ * (kv_heads * (head_dim + v_head_dim) * dtype_size).
+ * Returns SWA_ERR_CONFIG when N_swa <= window + page_size (the SWA pool
+ * cannot hold one request). Pure host function. */
+swa_status swa_pool_sizes(int64_t mem_bytes, int64_t F, int64_t S,
+                          int32_t L_full, int32_t L_swa, double r,
+                          int32_t page_size, int32_t window,
+                          int64_t *n_full, int64_t *n_swa);
+
+/* ------------------------------------------------------------- lifecycle --
+ * swa_state_bytes: size of the device state blob (mapping, free-page rings,
+ * staging lists, counters) for `cfg`; the caller allocates it (any
+ * contents, 256-byte aligned).
+ *
+ * swa_ctx_create: validates `cfg`, copies it, and initialises the blob on
+ * `stream`: mapping = 0 with the trailing -1 sentinel ([SWA note], "two
+ * pools and the mapping"); free lists = 1..num_pages, or the caller's
+ * permutation init_free_full / init_free_swa (device, num_pages entries,
+ * nullable).  ENVELOPE checks ([PR 34602], "implementation", step 2):
+ * row ids (num_pages+1)*2L*ps < 2^31 and a one-envelope tail pad; K and V
+ * widths are equal by construction (one head_dim).  Returns SWA_ERR_CONFIG
+ * for a rejected configuration, SWA_ERR_INVALID for null pointers. */
+size_t swa_state_bytes(const swa_config *cfg);
+swa_status swa_ctx_create(const swa_config *cfg, void *state_dev,
+                          const int64_t *init_free_full,
+                          const int64_t *init_free_swa, swa_stream_t stream,
+                          swa_ctx **out);
+void swa_ctx_destroy(swa_ctx *ctx);
+/* Message of the last failure on ctx (or of swa_ctx_create when ctx is
+ * NULL).  Valid until the next call on the same ctx. */
+const char *swa_last_error(const swa_ctx *ctx);
+swa_status swa_state_pointers(const swa_ctx *ctx, swa_state_view *out);
+
+/* Host mirrors, in tokens ([SWA note]: available = min of the two pools;
+ * [Pools 15]: staged pages count as free). */
+int64_t swa_available_size(const swa_ctx *ctx);
+int64_t swa_available_full(const swa_ctx *ctx);
+int64_t swa_available_swa(const swa_ctx *ctx);
+
+/* Synchronises `stream`, reads the error word into *err (0 = clean) and
+ * clears it.  Returns SWA_ERR_DEVICE_CHECK when *err != 0. */
+swa_status swa_device_check(swa_ctx *ctx, swa_stream_t stream, int32_t *err);
+/* Synchronises `stream` and reloads the host mirrors from the device
+ * counters (for callers that free without knowing page counts). */
+swa_status swa_sync_counts(swa_ctx *ctx, swa_stream_t stream);
+
+/* ------------------------------------------------------------ allocation --
+ * All three allocate the same number of slots in both pools and then write
+ * mapping[full] = swa ([SWA note], "two pools and the mapping").  Both
+ * pools are checked before either is touched; on SWA_ERR_NOMEM nothing
+ * changed except a need_sort merge, which the pages also run before the
+ * check ([Pools 15], "expansion and shortage", "_release_page_ids").
+ *
+ * swa_alloc: need_size (multiple of ps) slots of whole pages, written to
+ * out_full[need_size] (device), and out_swa when non-null. */
+swa_status swa_alloc(swa_ctx *ctx, int64_t need_size, int64_t *out_full,
+                     int64_t *out_swa, swa_stream_t stream);
+
+/* swa_alloc_extend ([Pools 15], "alloc_extend"): request b of bs extends
+ * from prefix_lens[b] to seq_lens[b] tokens.  Its slots follow its previous
+ * slot last_loc[b] (-1 when the prefix is empty) inside the half-full page,
+ * then fill new pages taken from the free list in request order.  Output
+ * out_full[sum(seq - pre)] in request order (out_swa likewise, nullable).
+ * last_loc may be NULL when req_to_token is given: it is then read as
+ * req_to_token[req_idx[b], pre-1] (or -1).  When req_to_token is non-null
+ * the new slots are also written to req_to_token[req_idx[b], pre..seq-1]
+ * (row stride rt_stride int32 elements).  The *_host arrays are host copies
+ * of prefix / seq lengths used for the page count. */
+swa_status swa_alloc_extend(swa_ctx *ctx, int32_t bs,
+                            const int64_t *prefix_lens, const int64_t *seq_lens,
+                            const int64_t *last_loc,
+                            const int64_t *prefix_lens_host,
+                            const int64_t *seq_lens_host, int64_t *out_full,
+                            int64_t *out_swa, int32_t *req_to_token,
+                            int64_t rt_stride, const int64_t *req_idx,
+                            swa_stream_t stream);
+
+/* swa_alloc_decode ([Pools 15], "alloc_decode"): one token per request,
+ * prefix = seq - 1: the slot is last_loc+1, or the first slot of a new page
+ * when the token opens a page.  Same argument conventions as
+ * swa_alloc_extend; out_full[bs]. */
+swa_status swa_alloc_decode(swa_ctx *ctx, int32_t bs, const int64_t *seq_lens,
+                            const int64_t *last_loc,
+                            const int64_t *seq_lens_host, int64_t *out_full,
+                            int64_t *out_swa, int32_t *req_to_token,
+                            int64_t rt_stride, const int64_t *req_idx,
+                            swa_stream_t stream);
+
+/* swa_translate: swa_loc[i] = full_to_swa[full_loc[i]], where full_loc -1
+ * reads the trailing sentinel (-1) ([SWA note], "attention backend":
+ * translate_loc_from_full_to_swa). */
+swa_status swa_translate(swa_ctx *ctx, const int64_t *full_loc, int64_t n,
+                         int64_t *swa_loc, swa_stream_t stream);
+
+/* --------------------------------------------------------------- release --
+ * swa_free ([SWA note], "two pools and the mapping"; [Pools 15], "free,
+ * dedupe and free_group"): frees the full pages of full_idx[n] (page ids
+ * deduplicated, in ascending order, prepended to the free list or staged
+ * under need_sort), then runs swa_free_swa on the same indices.
+ * n_full_pages / n_swa_pages: the caller's count of distinct pages each
+ * side will get back (it updates the host mirrors without a sync; a kernel
+ * that finds a different count sets SWA_DEVERR_COUNT).  Pass -1 when unknown
+ * and call swa_sync_counts() before the next capacity query. */
+swa_status swa_free(swa_ctx *ctx, const int64_t *full_idx, int64_t n,
+                    int64_t n_full_pages, int64_t n_swa_pages,
+                    swa_stream_t stream);
+/* swa_free_swa: frees the SWA pages of those full_idx whose mapping is > 0,
+ * then sets the mapping of every full_idx to 0, so calling it before
+ * swa_free never frees a page twice. */
+swa_status swa_free_swa(swa_ctx *ctx, const int64_t *full_idx, int64_t n,
+                        int64_t n_swa_pages, swa_stream_t stream);
+
+/* swa_evict_swa ([SWA note], "runtime: returning slid-out KV",
+ * free_swa_out_of_window_slots): for each request b (in batch order),
+ *   bound = pre_lens[b] - Wx            (radix == 0, chunk cache)
+ *         = pre_lens[b] - max(Wx, ps)   (radix != 0)
+ * with Wx the largest lookback of the model's SWA-pool layers (SLIDING: its
+ * window; CHUNKED: C-1).  With interval > 0 (decode) the pass skips the
+ * request unless bound - evicted[b] >= interval; interval == 0 always runs
+ * (before a prefill chunk).  new = floor(bound/ps)*ps,
+ * old = ceil(max(evicted[b], protected[b])/ps)*ps; if new > old the SWA
+ * pages of req_to_token[req_idx[b], old:new] are freed (one page id per ps
+ * positions, ascending within a request, later requests ahead of earlier
+ * ones - the order of per-request frees), their mapping entries set to 0,
+ * and evicted[b] = new.  Device arrays drive the kernel; the *_host arrays
+ * (same values) drive the host mirror, and evicted_host is updated too.
+ * protected may be NULL (all 0). */
+swa_status swa_evict_swa(swa_ctx *ctx, int32_t bs, const int32_t *req_to_token,
+                         int64_t rt_stride, const int64_t *req_idx,
+                         const int64_t *pre_lens, int64_t *evicted,
+                         const int64_t *protected_lens,
+                         const int64_t *pre_lens_host, int64_t *evicted_host,
+                         const int64_t *protected_host, int32_t interval,
+                         int32_t radix, swa_stream_t stream);
+
+/* ------------------------------------------------------------------ store --
+ * swa_store_kv ([Pools 15], "who writes into the pages", KVWriteLoc):
+ * k, v: [n][Hkv][D] rows of the new tokens of `layer` (f32 for an F32 pool,
+ * bf16 otherwise).  A FULL layer writes row i at full_loc[i]; other layers
+ * at swa_loc[i] (pre-translated once per batch; when NULL the mapping is
+ * read here).  E4M3 pools store round-to-nearest-even, saturating
+ * e4m3(x / scale) bytes ([Pools 15]: FP8 is kept as uint8). */
+swa_status swa_store_kv(swa_ctx *ctx, int32_t layer, const void *k,
+                        const void *v, int64_t n, const int64_t *full_loc,
+                        const int64_t *swa_loc, float k_scale, float v_scale,
+                        swa_stream_t stream);
+
+/* ------------------------------------------------------------------- plan --
+ * Per-batch translation done once and shared by every SWA-pool layer
+ * ([SWA note], "attention backend: translate once"): for request b it
+ * lists the SWA pages holding positions lo_b..hi_b, with
+ *   decode:  hi_b = seq_lens[b] - 1,  lo_b = max(0, hi_b - Wx)
+ *   extend:  hi_b = seq_lens[b] - 1,  lo_b = max(0, prefix_lens[b] - Wx)
+ * (Wx as in swa_evict_swa).  A position whose SWA mapping is 0 sets
+ * SWA_DEVERR_WINDOW_EVICTED.  `max_new` bounds seq - prefix over the batch
+ * (1 for decode).  swa_plan_bytes gives the workspace size. */
+size_t swa_plan_bytes(const swa_ctx *ctx, int32_t bs, int32_t max_new);
+swa_status swa_plan(swa_ctx *ctx, int32_t bs, const int32_t *req_to_token,
+                    int64_t rt_stride, const int64_t *req_idx,
+                    const int64_t *prefix_lens /* NULL = decode */,
+                    const int64_t *seq_lens, int32_t max_new, void *plan,
+                    size_t plan_bytes, swa_stream_t stream);
+
+/* ------------------------------------------------------------- attention --
+ * For a query at position p, query head h, KV head h / (Hq / Hkv), key set
+ * J (by layer kind, above), scale c and sink logit sigma_h ([SWA note],
+ * "design": learnable sink):
+ *   o_h = sum_j e^{c q.k_j - m} v_j / (e^{sigma_h - m} + sum_j e^{c q.k_j - m})
+ * sinks: [Hq] float logits, or NULL for no sink.  q, out: [n][Hq][D], f32
+ * for an F32 pool, bf16 otherwise.  E4M3 K/V are multiplied by k_scale /
+ * v_scale after decoding.  Keys of FULL layers are read through
+ * req_to_token, keys of SWA-pool layers through `plan` (built for the same
+ * batch).  Long key ranges are split across CTAs and merged in the same
+ * launch; `ws` is the split workspace (size from *_ws_bytes) and must be
+ * zero-filled before its first use (the kernels leave it reusable).
+ *
+ * swa_attn_decode: one query per request at p = seq_lens[b] - 1 (its KV
+ * already stored). max_seq_len bounds seq_lens (host; sizes the grid). */
+size_t swa_attn_decode_ws_bytes(const swa_ctx *ctx, int32_t layer, int32_t bs,
+                                int32_t max_seq_len);
+swa_status swa_attn_decode(swa_ctx *ctx, int32_t layer, int32_t bs,
+                           const int32_t *req_to_token, int64_t rt_stride,
+                           const int64_t *req_idx, const int64_t *seq_lens,
+                           int32_t max_seq_len, const void *plan, const void *q,
+                           const float *sinks, float sm_scale, float k_scale,
+                           float v_scale, void *out, void *ws, size_t ws_bytes,
+                           swa_stream_t stream);
+
+/* swa_attn_extend: chunked-prefill queries.  Request b owns query rows
+ * qo_indptr[b]..qo_indptr[b+1]-1 (device, bs+1 entries), at positions
+ * prefix_lens[b] .. seq_lens[b]-1, causal.  n_tokens = qo_indptr[bs] and
+ * max_new >= max(seq - prefix) are host values. */
+size_t swa_attn_extend_ws_bytes(const swa_ctx *ctx, int32_t layer,
+                                int64_t n_tokens, int32_t max_seq_len);
+swa_status swa_attn_extend(swa_ctx *ctx, int32_t layer, int32_t bs,
+                           const int32_t *req_to_token, int64_t rt_stride,
+                           const int64_t *req_idx, const int64_t *prefix_lens,
+                           const int64_t *seq_lens, const int64_t *qo_indptr,
+                           int64_t n_tokens, int32_t max_new,
+                           int32_t max_seq_len, const void *plan, const void *q,
+                           const float *sinks, float sm_scale, float k_scale,
+                           float v_scale, void *out, void *ws, size_t ws_bytes,
+                           swa_stream_t stream);
+
+/* Which kernel family the last attention call on ctx launched
+ * (0 = generic CUDA-core kernel, 1 = tensor-core decode, 2 = tcgen05
+ * extend), for tests and profiling. */
+int32_t swa_last_attn_path(const swa_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SWA_H */

@@ -1,0 +1,120 @@
+"""Workload-shaped parity: the GPU decode state (chunked prefill with eviction,
+then decode steps) against the oracle replaying the same call trace.
+
+Allocator state (mapping, free lists, req_to_token) is compared bit for bit;
+attention outputs of every layer against the oracle's brute-force softmax over
+the generator's K/V at the attended positions, after asserting (on the
+oracle's own mapping) that every attended SWA key is live."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+from hybrid_sliding_window_gb300 import api, synth  # noqa: E402
+from hybrid_sliding_window_gb300.workloads import SPECS, DecodeState, FULL, SLIDING, CHUNKED  # noqa: E402
+from oracle import allocator as OA  # noqa: E402
+from oracle import attention as OT  # noqa: E402
+from oracle import codecs as OC  # noqa: E402
+from tests.harness import assert_close  # noqa: E402
+
+OKIND = {FULL: OT.FULL, SLIDING: OT.SLIDING, CHUNKED: OT.CHUNKED}
+TOL = {"f32": 1e-5, "bf16": 2e-2, "e4m3": 2e-2}
+
+
+def replay(st: DecodeState):
+    """The oracle allocator driven by the GPU state's recorded calls."""
+    spec = st.spec
+    oa = OA.TwoPoolAllocator(st.size_full, st.size_swa, spec.ps)
+    ort = np.zeros(tuple(st.rt.shape), np.int64)
+    for op in st.trace:
+        if op[0] == "evict":
+            _, rows, pre, ev, interval = op
+            OA.evict_swa(oa, ort, rows, pre, ev, [0] * len(rows), spec.lookback(), interval)
+        else:
+            if op[0] == "extend":
+                _, rows, pre, seq = op
+            else:
+                _, rows, seq = op
+                pre = [s - 1 for s in seq]
+            last = [int(ort[r, p - 1]) if p > 0 else -1 for r, p in zip(rows, pre)]
+            full, _ = oa.alloc_extend(pre, seq, last)
+            off = 0
+            for r, p, s in zip(rows, pre, seq):
+                ort[r, p:s] = full[off:off + s - p]
+                off += s - p
+    return oa, ort
+
+
+def check_state(st, oa, ort):
+    torch.cuda.synchronize()
+    assert api.swa_device_check(st.ctx) == 0
+    np.testing.assert_array_equal(st.ctx.mapping().cpu().numpy(), np.array(oa.mapping, np.int64))
+    for full, led in ((True, oa.full), (False, oa.swa)):
+        free, _ = st.ctx.free_list(full)
+        assert free == led.free
+    np.testing.assert_array_equal(st.rt.cpu().numpy().astype(np.int64), ort)
+    assert api.swa_available_size(st.ctx) == oa.available_size()
+
+
+def oracle_decode(st, oa, ort, layer, b, seq_b, q_row):
+    """Oracle output [Hq, D] for batch entry b at position seq_b - 1."""
+    spec = st.spec
+    kind, w, hkv = spec.layers[layer]
+    p = int(seq_b) - 1
+    row = int(st.rows[b])
+    J = list(OT.key_positions(OKIND[kind], w, p))
+    if kind != FULL:
+        assert all(oa.mapping[int(ort[row, j])] > 0 for j in J), "evicted key in window"
+    bf = spec.dtype != "f32"
+    K = synth.tokens(spec.seed, synth.STREAM_K, layer, [row] * len(J), J, hkv, spec.D, bf16=bf)
+    V = synth.tokens(spec.seed, synth.STREAM_V, layer, [row] * len(J), J, hkv, spec.D, bf16=bf)
+    if spec.dtype == "e4m3":
+        K = OC.e4m3_decode(OC.e4m3_encode(K))
+        V = OC.e4m3_decode(OC.e4m3_encode(V))
+    return OT.attend_heads(q_row.astype(np.float64), K, V, st.sinks_h[layer], st.scale)
+
+
+def run_small(spec, steps=3, layers=None, requests=None):
+    st = DecodeState(spec, max_steps=steps + 2, trace=True, poison_page0=True)
+    st.prefill()
+    st.alloc_decode_buffers()
+    inputs = st.make_decode_inputs(steps)
+    for s in range(steps):
+        st.decode_step(inputs[s])
+    oa, ort = replay(st)
+    check_state(st, oa, ort)
+    last = inputs[-1]
+    for l in (layers if layers is not None else range(len(spec.layers))):
+        g = st.outs[l].float().cpu().numpy()
+        q = last["q"][l].float().cpu().numpy()
+        for b in (requests if requests is not None else range(st.B)):
+            o = oracle_decode(st, oa, ort, l, b, last["seq_h"][b], q[b])
+            assert_close(g[b], o, TOL[spec.dtype], f"{spec.name} layer {l} req {b}")
+    return st
+
+
+def small(name, **kw):
+    return dataclasses.replace(SPECS[name], **kw)
+
+
+def test_mimo_shaped_small():
+    spec = small("mimo", layers=SPECS["mimo"].layers[:10], batch=4, seq_kind="uniform",
+                 seq_lo=100, seq_hi=1500, chunk=256, interval=64)
+    run_small(spec, steps=70)          # crosses an eviction interval and page boundaries
+
+
+def test_gptoss_shaped_small():
+    spec = small("gptoss", layers=SPECS["gptoss"].layers[:4], batch=6, seq_lo=200, seq_hi=3000,
+                 chunk=512, interval=16)
+    run_small(spec, steps=20)
+
+
+def test_llama4_shaped_small_envelope_fp8():
+    spec = small("llama4", layers=[(CHUNKED, 256, 8), (CHUNKED, 256, 8), (FULL, 0, 8)] * 2,
+                 batch=3, seq_kind="uniform", seq_lo=300, seq_hi=1300, chunk=256, interval=32)
+    run_small(spec, steps=40)
