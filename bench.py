@@ -164,6 +164,16 @@ def run_native(args, rank, world):
     torch.cuda.set_device(local)
     api.lib()
     spec = SPECS[args.workload]
+    if args.batch or args.layers or args.r or args.chunk:
+        # Reduced shapes for profiler captures only (named in the config line).
+        import dataclasses
+        spec = dataclasses.replace(
+            spec, batch=args.batch or spec.batch,
+            layers=spec.layers[:args.layers] if args.layers else spec.layers,
+            r=args.r or spec.r, chunk=args.chunk or spec.chunk,
+            description=spec.description + f" [reduced: batch={args.batch or spec.batch}, "
+                                           f"layers={args.layers or len(spec.layers)}, "
+                                           f"r={args.r or spec.r}, chunk={args.chunk or spec.chunk}]")
     W, K = args.warmup, args.steps
     st = DecodeState(spec, max_steps=W + 2 * K + 4)
     t0 = time.time()
@@ -339,6 +349,10 @@ def main():
     ap.add_argument("--workload", default="mimo", choices=["mimo", "gptoss", "llama4"])
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--batch", type=int, default=0, help="reduced batch (profiling only)")
+    ap.add_argument("--layers", type=int, default=0, help="first N layers (profiling only)")
+    ap.add_argument("--r", type=float, default=0.0, help="SWA/full token ratio (profiling only)")
+    ap.add_argument("--chunk", type=int, default=0, help="prefill chunk (profiling only)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))

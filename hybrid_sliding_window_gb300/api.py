@@ -90,6 +90,7 @@ SIGNATURES = {
     "swa_attn_extend": (I32, [P, I32, I32, P, I64, P, P, P, P, I64, I32, I32, P, P, P, F32, F32,
                               F32, P, P, SZ, P]),
     "swa_last_attn_path": (I32, [P]),
+    "swa_set_attn_path": (I32, [P, I32]),
     "swa_synth_tokens": (I32, [C.c_uint64, I32, I32, P, P, I64, I32, I32, I32, P, P]),
 }
 
@@ -364,6 +365,10 @@ def swa_attn_extend(ctx, layer, req_to_token, req_idx, prefix_lens, seq_lens, qo
 
 def swa_last_attn_path(ctx):
     return lib().swa_last_attn_path(ctx.handle)
+
+
+def swa_set_attn_path(ctx, path):
+    _check(lib().swa_set_attn_path(ctx.handle, path), ctx.handle)
 
 
 def swa_synth_tokens(seed, stream_id, layer, req, pos, heads, dim, out, stream=None):

@@ -1,10 +1,550 @@
-// Tensor-core paged decode attention (placeholder: not yet selected).
+// Tensor-core paged decode attention for bf16 and FP8-E4M3 KV (D = 64 / 128,
+// GQA group G <= 16).
+//
+// Method: "SWA in SGLang" design note - sliding layers read the window of
+// Wx+1 keys through the per-batch SWA page table, full layers every key
+// through req_to_token; a per-head sink logit joins the denominator.
+//
+// GB300 design.  Decode is bound by HBM: each key costs 4*D*G flops per KV
+// head on 2*D*b bytes, i.e. 2G/b flop/byte (16 for MiMo's full layers), which
+// CUDA-core FMAs cannot sustain at HBM speed, so the QK^T and PV products run
+// on tensor cores with the G query heads of one KV head as the M=16 rows of
+// mma.m16n8k16 (unused rows are zero).  Work item = (request, KV head, split
+// of up to 1024 keys); a CTA of 4 warps streams 64-key tiles through a
+// 3-stage cp.async pipeline (16-byte gathers of whole K/V rows, row address
+// from the index tables, out-of-range rows zero-filled without a read), each
+// warp owning 16 keys of every tile with its own online-softmax state in
+// registers.  FP8 tiles are widened to f16 in shared memory (E4M3 is a subset
+// of f16; the scales fold into the score scale and the output).  Splits of
+// one (request, KV head) meet through an atomic ticket: the last CTA merges
+// the partials and the sink, so one launch does split and merge.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
 #include "swa_internal.h"
 
 namespace swa {
-bool mma_decode_supported(const Ctx &, int) { return false; }
-size_t mma_decode_ws_bytes(const Ctx &, int, int64_t, int) { return 0; }
-cudaError_t launch_attn_decode_mma(Ctx &, const AttnArgs &, cudaStream_t) {
-  return cudaErrorNotSupported;
+namespace {
+
+constexpr int kTile = 64;
+constexpr int kWarps = 4;
+constexpr int kStages = 3;
+constexpr int kSplitKeys = 1024;
+
+struct MmaParams {
+  int kind, window, hkv, G, ps;
+  int ps_shift;          // log2(ps) when ps is a power of two, else -1
+  KvAddr addr;
+  int64_t pool_rows;
+  const int32_t *rt;
+  int64_t rt_stride;
+  const int64_t *req_idx;
+  const int64_t *seq;
+  PlanView plan;
+  const __nv_bfloat16 *q;
+  const float *sinks;
+  float qk_scale_log2;   // sm_scale * log2(e) * k_scale
+  float v_scale;
+  __nv_bfloat16 *out;
+  float *partials;
+  int32_t *tickets;
+  int max_splits;
+  int32_t *err;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
 }
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool pred) {
+  int sz = pred ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(sz));
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  if constexpr (F16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (F16) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+  }
+}
+
+__device__ __forceinline__ int64_t key_slot(const MmaParams &P, int b, int64_t j) {
+  if (P.kind == SWA_LAYER_FULL) return P.rt[P.req_idx[b] * P.rt_stride + j];
+  const int32_t *h = P.plan.hdr + b * 4;
+  const int64_t k = j / P.ps - h[2];
+  if (j < h[0] || k < 0 || k >= h[3]) {
+    set_error(P.err, SWA_DEVERR_RANGE);
+    return 0;
+  }
+  const int64_t page = P.plan.pages[(int64_t)b * P.plan.max_pages + k];
+  if (page <= 0) set_error(P.err, SWA_DEVERR_WINDOW_EVICTED);
+  return page * P.ps + j % P.ps;
+}
+
+// Shared-memory plan (bytes):
+//   Q tile      16 x D  16-bit, swizzled                      : 32*D
+//   stages      kStages x (K,V) 64 x D stored elements         : kStages*2*64*D*esz
+//   FP8 only:   widened K,V tile 64 x D f16, swizzled          : 2*64*D*2
+template <int D, bool FP8>
+struct Smem {
+  static constexpr int kEsz = FP8 ? 1 : 2;
+  static constexpr int kQ = 16 * D * 2;
+  static constexpr int kStageBytes = 2 * kTile * D * kEsz;
+  static constexpr int kWide = FP8 ? 2 * kTile * D * 2 : 0;
+  static constexpr int kMerge = kWarps * 16 * (D + 4) * 4 + 2 * kWarps * 16 * 4;
+  static constexpr int kMain = kQ + kStages * kStageBytes + kWide;
+  static constexpr int kTotal = kMain > kMerge ? kMain : kMerge;
+};
+
+// 16-bit tile addressing: row r, 16-byte chunk c (D/8 chunks per row), XOR swizzle.
+template <int D>
+__device__ __forceinline__ int swz(int r, int c) {
+  return r * (D * 2) + ((c ^ (r & 7)) << 4);
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kWarps * 32, 2) k_decode_mma(MmaParams P) {
+  using S = Smem<D, FP8>;
+  constexpr bool F16 = FP8;                 // FP8 KV widens to f16; bf16 KV stays bf16
+  constexpr int kEsz = S::kEsz;
+  constexpr int kRowChunks = D * kEsz / 16; // 16-byte chunks of one stored head row
+  extern __shared__ __align__(128) char smem[];
+  char *sq = smem;
+  char *sstage = smem + S::kQ;
+  char *swide = sstage + kStages * S::kStageBytes;
+
+  // KV heads fastest: the CTAs of all heads of the same keys run together, so
+  // each token's interleaved head rows are read from DRAM at about one time.
+  const int kvh = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = P.G;
+  const int64_t p = P.seq[b] - 1;
+  int64_t lo = 0;
+  if (P.kind == SWA_LAYER_SLIDING) lo = p - P.window > 0 ? p - P.window : 0;
+  else if (P.kind == SWA_LAYER_CHUNKED) lo = (p / P.window) * P.window;
+  const int64_t n_keys = p - lo + 1;
+  const int n_splits = (int)((n_keys + kSplitKeys - 1) / kSplitKeys);
+  if (split >= n_splits) return;
+  const int64_t k0 = lo + (int64_t)split * kSplitKeys;
+  const int64_t k1 = min(p + 1, k0 + kSplitKeys);
+  const int n_tiles = (int)((k1 - k0 + kTile - 1) / kTile);
+
+  // ---- Q tile (rows >= G zero) ----
+  const int Hq = P.hkv * G;
+  for (int i = tid; i < 16 * (D / 8); i += blockDim.x) {
+    const int r = i / (D / 8), c = i % (D / 8);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < G) {
+      v = *reinterpret_cast<const uint4 *>(P.q + ((int64_t)b * Hq + kvh * G + r) * D + c * 8);
+      if constexpr (F16) {
+        __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(&v);
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[e] = pack2<true>(__bfloat162float(h[2 * e]), __bfloat162float(h[2 * e + 1]));
+        v = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+    *reinterpret_cast<uint4 *>(sq + swz<D>(r, c)) = v;
+  }
+
+  // ---- page rows of this split, looked up once (one table read per page) ----
+  // Positions of one page occupy consecutive slots of one pool page, so the
+  // row of key j is rowbase[j / ps - pg0] + j % ps.
+  int64_t *s_rb = reinterpret_cast<int64_t *>(smem + S::kTotal);
+  const int64_t pg0 = k0 / P.ps;
+  const int n_pg = (int)((k1 - 1) / P.ps - pg0 + 1);
+  const int64_t page_stride = (int64_t)P.ps * (P.addr.blocks ? P.addr.blocks : 1);
+  const int64_t max_page = (P.pool_rows / P.ps) - 1;
+  for (int i = tid; i < n_pg; i += blockDim.x) {
+    const int64_t pos = (pg0 + i) * P.ps > k0 ? (pg0 + i) * P.ps : k0;
+    const int64_t slot = key_slot(P, b, pos);
+    int64_t page = slot / P.ps;
+    if (slot < 0 || page > max_page) {
+      set_error(P.err, SWA_DEVERR_RANGE);
+      page = 0;
+    }
+    s_rb[i] = page * page_stride;
+  }
+
+  // ---- tile loader ----
+  const char *kbase = P.addr.k + (int64_t)kvh * D * kEsz;
+  const char *vbase = P.addr.v + (int64_t)kvh * D * kEsz;
+  const int ps_shift = P.ps_shift;
+  auto load_tile = [&](int t) {
+    char *st = sstage + (t % kStages) * S::kStageBytes;
+    const int64_t kt = k0 + (int64_t)t * kTile;
+    for (int i = tid; i < kTile * kRowChunks; i += blockDim.x) {
+      const int r = i / kRowChunks, c = i % kRowChunks;
+      const int64_t j = kt + r;
+      const bool ok = j < k1;
+      int64_t off = 0;
+      if (ok) {
+        int64_t pg, in;
+        if (ps_shift >= 0) {
+          pg = j >> ps_shift;
+          in = j & ((1 << ps_shift) - 1);
+        } else {
+          pg = j / P.ps;
+          in = j % P.ps;
+        }
+        off = (s_rb[pg - pg0] + in) * P.addr.row_bytes + c * 16;
+      }
+      int dk, dv;
+      if constexpr (FP8) {
+        dk = r * D + c * 16;                         // raw bytes, not swizzled
+        dv = kTile * D + r * D + c * 16;
+      } else {
+        dk = swz<D>(r, c);
+        dv = kTile * D * 2 + swz<D>(r, c);
+      }
+      cp_async16(smem_u32(st + dk), kbase + off, ok);
+      cp_async16(smem_u32(st + dv), vbase + off, ok);
+    }
+  };
+
+  __syncthreads();  // Q tile and page rows visible
+#pragma unroll
+  for (int t = 0; t < kStages - 1; ++t) {
+    if (t < n_tiles) load_tile(t);
+    cp_commit();
+  }
+
+  uint32_t qa[D / 16][4];
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int c = ks * 2 + (lane >> 4);
+    ldsm_x4(smem_u32(sq + swz<D>(r, c)), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+  }
+
+  float o[D / 8][4];
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const int g = lane >> 2, c4 = lane & 3;
+
+  for (int t = 0; t < n_tiles; ++t) {
+    cp_wait<kStages - 2>();
+    __syncthreads();
+    if (t + kStages - 1 < n_tiles) load_tile(t + kStages - 1);
+    cp_commit();
+    const char *st = sstage + (t % kStages) * S::kStageBytes;
+    const char *tk;
+    const char *tv;
+    if constexpr (FP8) {
+      // Widen this tile to f16 (swizzled), 8 elements per thread-step.
+      for (int i = tid; i < 2 * kTile * (D / 8); i += blockDim.x) {
+        const int half = i / (kTile * (D / 8));
+        const int rem = i % (kTile * (D / 8));
+        const int r = rem / (D / 8), c = rem % (D / 8);
+        const uint2 raw = *reinterpret_cast<const uint2 *>(st + half * kTile * D + r * D + c * 8);
+        const __nv_fp8x2_storage_t *f = reinterpret_cast<const __nv_fp8x2_storage_t *>(&raw);
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(f[e], __NV_E4M3);
+          w[e] = (uint32_t)hr.x | ((uint32_t)hr.y << 16);
+        }
+        *reinterpret_cast<uint4 *>(swide + half * kTile * D * 2 + swz<D>(r, c)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      __syncthreads();
+      tk = swide;
+      tv = swide + kTile * D * 2;
+    } else {
+      tk = st;
+      tv = st + kTile * D * 2;
+    }
+    // S = Q K^T for this warp's 16 keys.
+    float s[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < D / 32; ++kk) {
+        const int r = warp * 16 + nt * 8 + (lane & 7);
+        const int c = kk * 4 + (lane >> 3);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(smem_u32(tk + swz<D>(r, c)), b0, b1, b2, b3);
+        mma16816<F16>(s[nt], qa[2 * kk], b0, b1);
+        mma16816<F16>(s[nt], qa[2 * kk + 1], b2, b3);
+      }
+    }
+    // Scale, mask, online softmax (rows g and g+8).
+    const int64_t kbase_j = k0 + (int64_t)t * kTile + warp * 16;
+    float rmax0 = -INFINITY, rmax1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int64_t j = kbase_j + nt * 8 + 2 * c4 + (e & 1);
+        float v = s[nt][e] * P.qk_scale_log2;
+        if (j >= k1) v = -INFINITY;
+        s[nt][e] = v;
+      }
+      rmax0 = fmaxf(rmax0, fmaxf(s[nt][0], s[nt][1]));
+      rmax1 = fmaxf(rmax1, fmaxf(s[nt][2], s[nt][3]));
+    }
+    rmax0 = fmaxf(rmax0, __shfl_xor_sync(0xffffffffu, rmax0, 1));
+    rmax0 = fmaxf(rmax0, __shfl_xor_sync(0xffffffffu, rmax0, 2));
+    rmax1 = fmaxf(rmax1, __shfl_xor_sync(0xffffffffu, rmax1, 1));
+    rmax1 = fmaxf(rmax1, __shfl_xor_sync(0xffffffffu, rmax1, 2));
+    const float mn0 = fmaxf(m0, rmax0), mn1 = fmaxf(m1, rmax1);
+    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float corr0 = exp2f(m0 - mu0), corr1 = exp2f(m1 - mu1);
+    m0 = mn0;
+    m1 = mn1;
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      s[nt][0] = exp2f(s[nt][0] - mu0);
+      s[nt][1] = exp2f(s[nt][1] - mu0);
+      s[nt][2] = exp2f(s[nt][2] - mu1);
+      s[nt][3] = exp2f(s[nt][3] - mu1);
+      ps0 += s[nt][0] + s[nt][1];
+      ps1 += s[nt][2] + s[nt][3];
+    }
+    l0 = l0 * corr0 + ps0;
+    l1 = l1 * corr1 + ps1;
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      o[n][0] *= corr0;
+      o[n][1] *= corr0;
+      o[n][2] *= corr1;
+      o[n][3] *= corr1;
+    }
+    uint32_t pa[4];
+    pa[0] = pack2<F16>(s[0][0], s[0][1]);
+    pa[1] = pack2<F16>(s[0][2], s[0][3]);
+    pa[2] = pack2<F16>(s[1][0], s[1][1]);
+    pa[3] = pack2<F16>(s[1][2], s[1][3]);
+    // O += P V.
+#pragma unroll
+    for (int dp = 0; dp < D / 16; ++dp) {
+      const int r = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int c = dp * 2 + (lane >> 4);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(smem_u32(tv + swz<D>(r, c)), b0, b1, b2, b3);
+      mma16816<F16>(o[2 * dp], pa, b0, b1);
+      mma16816<F16>(o[2 * dp + 1], pa, b2, b3);
+    }
+  }
+  cp_wait<0>();
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  __syncthreads();  // stages no longer needed: reuse for the warp merge
+
+  constexpr int OS = D + 4;
+  float *sm_o = reinterpret_cast<float *>(smem);
+  float *sm_m = sm_o + kWarps * 16 * OS;
+  float *sm_l = sm_m + kWarps * 16;
+  if (c4 == 0) {
+    sm_m[warp * 16 + g] = m0;
+    sm_m[warp * 16 + g + 8] = m1;
+    sm_l[warp * 16 + g] = l0;
+    sm_l[warp * 16 + g + 8] = l1;
+  }
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) {
+    float *r0p = sm_o + (warp * 16 + g) * OS + n * 8 + 2 * c4;
+    float *r1p = sm_o + (warp * 16 + g + 8) * OS + n * 8 + 2 * c4;
+    r0p[0] = o[n][0];
+    r0p[1] = o[n][1];
+    r1p[0] = o[n][2];
+    r1p[1] = o[n][3];
+  }
+  __syncthreads();
+
+  const bool single = n_splits == 1;
+  const int stride = G * (D + 2);
+  const int64_t item = ((int64_t)b * P.hkv + kvh) * P.max_splits + split;
+  float *part = P.partials + item * stride;
+  for (int e = tid; e < G * D; e += blockDim.x) {
+    const int gg = e / D, d = e % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * 16 + gg]);
+    const float Mu = M == -INFINITY ? 0.f : M;
+    float L = 0.f, A = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = exp2f(sm_m[w * 16 + gg] - Mu);
+      L += sm_l[w * 16 + gg] * f;
+      A += sm_o[(w * 16 + gg) * OS + d] * f;
+    }
+    if (single) {
+      float Mf = Mu, extra = 0.f;
+      if (P.sinks) {
+        const float sg = P.sinks[kvh * G + gg] * 1.4426950408889634f;
+        Mf = fmaxf(Mu, sg);
+        extra = exp2f(sg - Mf);
+      }
+      const float r = exp2f(Mu - Mf);
+      P.out[((int64_t)b * Hq + kvh * G + gg) * D + d] =
+          __float2bfloat16_rn(A * r * P.v_scale / (L * r + extra));
+    } else {
+      part[gg * (D + 2) + 2 + d] = A;
+      if (d == 0) {
+        part[gg * (D + 2)] = Mu;
+        part[gg * (D + 2) + 1] = L;
+      }
+    }
+  }
+  if (single) return;
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = atomicAdd(&P.tickets[(int64_t)b * P.hkv + kvh], 1);
+    s_last = prev == n_splits - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const float *base = P.partials + ((int64_t)b * P.hkv + kvh) * P.max_splits * stride;
+  for (int e = tid; e < G * D; e += blockDim.x) {
+    const int gg = e / D, d = e % D;
+    float M = -INFINITY;
+    for (int s = 0; s < n_splits; ++s) M = fmaxf(M, __ldcg(base + s * stride + gg * (D + 2)));
+    float Mf = M, extra = 0.f;
+    if (P.sinks) {
+      const float sg = P.sinks[kvh * G + gg] * 1.4426950408889634f;
+      Mf = fmaxf(M, sg);
+      extra = exp2f(sg - Mf);
+    }
+    float L = extra, A = 0.f;
+    for (int s = 0; s < n_splits; ++s) {
+      const float *q = base + s * stride + gg * (D + 2);
+      const float f = exp2f(__ldcg(q) - Mf);
+      L += __ldcg(q + 1) * f;
+      A += __ldcg(q + 2 + d) * f;
+    }
+    P.out[((int64_t)b * Hq + kvh * G + gg) * D + d] = __float2bfloat16_rn(A * P.v_scale / L);
+  }
+  if (tid == 0) P.tickets[(int64_t)b * P.hkv + kvh] = 0;
+}
+
+int max_keys_of(const Ctx &c, int layer, int max_seq_len) {
+  const LayerInfo &L = c.layers[layer];
+  int64_t mk = max_seq_len;
+  if (L.kind == SWA_LAYER_SLIDING && L.window + 1 < mk) mk = L.window + 1;
+  if (L.kind == SWA_LAYER_CHUNKED && L.window < mk) mk = L.window;
+  return (int)(mk < 1 ? 1 : mk);
+}
+
+struct Layout {
+  size_t ticket_off, total;
+  int max_splits;
+};
+
+Layout layout_of(const Ctx &c, int layer, int64_t nq, int max_seq_len) {
+  Layout w;
+  const LayerInfo &L = c.layers[layer];
+  const int G = c.cfg.num_q_heads / L.hkv;
+  w.max_splits = (max_keys_of(c, layer, max_seq_len) + kSplitKeys - 1) / kSplitKeys;
+  size_t part = (size_t)nq * L.hkv * w.max_splits * G * (c.cfg.head_dim + 2) * sizeof(float);
+  w.ticket_off = (part + 255) / 256 * 256;
+  w.total = w.ticket_off + ((size_t)nq * L.hkv * sizeof(int32_t) + 255) / 256 * 256;
+  return w;
+}
+
+template <int D, bool FP8>
+cudaError_t launch_t(dim3 grid, const MmaParams &P, cudaStream_t s) {
+  // Main tiles (or merge scratch), then the split's page-row table.
+  const int smem = Smem<D, FP8>::kTotal + (kSplitKeys / P.ps + 2) * (int)sizeof(int64_t);
+  cudaError_t e = cudaFuncSetAttribute(k_decode_mma<D, FP8>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  k_decode_mma<D, FP8><<<grid, kWarps * 32, smem, s>>>(P);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool mma_decode_supported(const Ctx &c, int layer) {
+  if (c.cfg.kv_dtype != SWA_DTYPE_BF16 && c.cfg.kv_dtype != SWA_DTYPE_E4M3) return false;
+  if (c.cfg.head_dim != 64 && c.cfg.head_dim != 128) return false;
+  const int G = c.cfg.num_q_heads / c.layers[layer].hkv;
+  return G >= 1 && G <= 16;
+}
+
+size_t mma_decode_ws_bytes(const Ctx &c, int layer, int64_t nq, int max_seq_len) {
+  return layout_of(c, layer, nq, max_seq_len).total;
+}
+
+cudaError_t launch_attn_decode_mma(Ctx &c, const AttnArgs &a, cudaStream_t s) {
+  if (a.nq == 0) return cudaSuccess;
+  const LayerInfo &L = c.layers[a.layer];
+  Layout w = layout_of(c, a.layer, a.nq, a.max_seq_len);
+  MmaParams P;
+  P.kind = L.kind;
+  P.window = L.window;
+  P.hkv = L.hkv;
+  P.G = c.cfg.num_q_heads / L.hkv;
+  P.ps = c.cfg.page_size;
+  P.ps_shift = (P.ps & (P.ps - 1)) == 0 ? __builtin_ctz((unsigned)P.ps) : -1;
+  P.addr = L.addr;
+  P.pool_rows = (L.in_full ? c.cfg.size_full : c.cfg.size_swa) + c.cfg.page_size;
+  P.rt = a.rt;
+  P.rt_stride = a.rt_stride;
+  P.req_idx = a.req_idx;
+  P.seq = a.seq;
+  P.plan = a.plan;
+  P.q = static_cast<const __nv_bfloat16 *>(a.q);
+  P.sinks = a.sinks;
+  const bool fp8 = c.cfg.kv_dtype == SWA_DTYPE_E4M3;
+  P.qk_scale_log2 = a.scale * 1.4426950408889634f * (fp8 ? a.k_scale : 1.f);
+  P.v_scale = fp8 ? a.v_scale : 1.f;
+  P.out = static_cast<__nv_bfloat16 *>(a.out);
+  P.partials = static_cast<float *>(a.ws);
+  P.tickets = reinterpret_cast<int32_t *>(static_cast<char *>(a.ws) + w.ticket_off);
+  P.max_splits = w.max_splits;
+  P.err = c.err_word;
+  dim3 grid(L.hkv, w.max_splits, a.nq);
+  const int D = c.cfg.head_dim;
+  if (D == 128) return fp8 ? launch_t<128, true>(grid, P, s) : launch_t<128, false>(grid, P, s);
+  return fp8 ? launch_t<64, true>(grid, P, s) : launch_t<64, false>(grid, P, s);
+}
+
 }  // namespace swa

@@ -326,8 +326,9 @@ cudaError_t launch_attn_simt(Ctx &c, const AttnArgs &a, cudaStream_t s) {
   P.q = a.q;
   P.sinks = a.sinks;
   P.scale_log2 = a.scale * 1.4426950408889634f;
-  P.k_scale = a.k_scale;
-  P.v_scale = a.v_scale;
+  // Scales apply to decoded E4M3 values only.
+  P.k_scale = c.cfg.kv_dtype == SWA_DTYPE_E4M3 ? a.k_scale : 1.f;
+  P.v_scale = c.cfg.kv_dtype == SWA_DTYPE_E4M3 ? a.v_scale : 1.f;
   P.out = a.out;
   P.partials = static_cast<float *>(a.ws);
   P.tickets = reinterpret_cast<int32_t *>(static_cast<char *>(a.ws) + w.ticket_off);

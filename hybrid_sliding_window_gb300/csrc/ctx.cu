@@ -14,6 +14,7 @@
 
 struct swa_ctx : public swa::Ctx {
   bool mirror_stale = false;
+  int forced_path = -1;
 };
 
 namespace {
@@ -483,7 +484,12 @@ swa_status swa_plan(swa_ctx *c, int32_t bs, const int32_t *rt, int64_t rt_stride
 }
 
 // --------------------------------------------------------------- attention ---
-static bool use_mma(const swa_ctx *c, int layer) { return swa::mma_decode_supported(*c, layer); }
+static bool use_mma(const swa_ctx *c, int layer) {
+  return c->forced_path != 0 && swa::mma_decode_supported(*c, layer);
+}
+static bool use_tc(const swa_ctx *c, int layer) {
+  return c->forced_path != 0 && swa::tc_extend_supported(*c, layer);
+}
 
 size_t swa_attn_decode_ws_bytes(const swa_ctx *c, int32_t layer, int32_t bs, int32_t max_seq_len) {
   if (!c || layer < 0 || layer >= c->cfg.num_layers || bs < 0 || max_seq_len < 1) return 0;
@@ -540,8 +546,7 @@ swa_status swa_attn_decode(swa_ctx *c, int32_t layer, int32_t bs, const int32_t 
 size_t swa_attn_extend_ws_bytes(const swa_ctx *c, int32_t layer, int64_t n_tokens,
                                 int32_t max_seq_len) {
   if (!c || layer < 0 || layer >= c->cfg.num_layers || n_tokens < 0 || max_seq_len < 1) return 0;
-  if (swa::tc_extend_supported(*c, layer))
-    return swa::tc_extend_ws_bytes(*c, layer, n_tokens, max_seq_len);
+  if (use_tc(c, layer)) return swa::tc_extend_ws_bytes(*c, layer, n_tokens, max_seq_len);
   return swa::simt_ws_bytes(*c, layer, n_tokens, max_seq_len);
 }
 
@@ -561,7 +566,7 @@ swa_status swa_attn_extend(swa_ctx *c, int32_t layer, int32_t bs, const int32_t 
     return fail(c, SWA_ERR_INVALID, "bad attention args");
   if (ws_bytes < swa_attn_extend_ws_bytes(c, layer, n_tokens, max_seq_len) || !ws)
     return fail(c, SWA_ERR_INVALID, "split workspace too small");
-  const bool tc = swa::tc_extend_supported(*c, layer);
+  const bool tc = use_tc(c, layer);
   if (!tc && n_tokens > 65535) return fail(c, SWA_ERR_INVALID, "n_tokens > 65535 on the generic path");
   swa::AttnArgs a{};
   a.layer = layer;
@@ -596,5 +601,12 @@ swa_status swa_attn_extend(swa_ctx *c, int32_t layer, int32_t bs, const int32_t 
 }
 
 int32_t swa_last_attn_path(const swa_ctx *c) { return c ? c->last_path : -1; }
+
+swa_status swa_set_attn_path(swa_ctx *c, int32_t path) {
+  if (!c) return SWA_ERR_INVALID;
+  if (path != -1 && path != 0) return fail(c, SWA_ERR_INVALID, "path must be -1 or 0");
+  c->forced_path = path;
+  return SWA_OK;
+}
 
 }  // extern "C"

@@ -58,8 +58,11 @@ class Spec:
     sinks: bool = True
     chunk: int = 8192
     description: str = ""
+    seq_list: tuple = None   # explicit lengths (overrides seq_kind)
 
     def seq_lens(self) -> np.ndarray:
+        if self.seq_list is not None:
+            return np.asarray(self.seq_list, dtype=np.int64)
         if self.seq_kind == "uniform":
             return synth.seq_lens_uniform(self.seed, self.batch, self.seq_lo, self.seq_hi)
         if self.seq_kind == "loguniform":

@@ -340,6 +340,10 @@ swa_status swa_attn_extend(swa_ctx *ctx, int32_t layer, int32_t bs,
  * (0 = generic CUDA-core kernel, 1 = tensor-core decode, 2 = tcgen05
  * extend), for tests and profiling. */
 int32_t swa_last_attn_path(const swa_ctx *ctx);
+/* Restricts the kernel family attention calls on ctx may take: -1 = best
+ * available (default), 0 = generic CUDA-core kernel only.  Any other value
+ * is SWA_ERR_INVALID.  For tests and profiling. */
+swa_status swa_set_attn_path(swa_ctx *ctx, int32_t path);
 
 #ifdef __cplusplus
 }

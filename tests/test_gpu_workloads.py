@@ -79,8 +79,9 @@ def oracle_decode(st, oa, ort, layer, b, seq_b, q_row):
     return OT.attend_heads(q_row.astype(np.float64), K, V, st.sinks_h[layer], st.scale)
 
 
-def run_small(spec, steps=3, layers=None, requests=None):
+def run_small(spec, steps=3, layers=None, requests=None, path=-1, expect_path=None):
     st = DecodeState(spec, max_steps=steps + 2, trace=True, poison_page0=True)
+    api.swa_set_attn_path(st.ctx, path)
     st.prefill()
     st.alloc_decode_buffers()
     inputs = st.make_decode_inputs(steps)
@@ -95,6 +96,8 @@ def run_small(spec, steps=3, layers=None, requests=None):
         for b in (requests if requests is not None else range(st.B)):
             o = oracle_decode(st, oa, ort, l, b, last["seq_h"][b], q[b])
             assert_close(g[b], o, TOL[spec.dtype], f"{spec.name} layer {l} req {b}")
+    if expect_path is not None:
+        assert api.swa_last_attn_path(st.ctx) == expect_path
     return st
 
 
@@ -102,19 +105,46 @@ def small(name, **kw):
     return dataclasses.replace(SPECS[name], **kw)
 
 
-def test_mimo_shaped_small():
+PATHS = [pytest.param(-1, 1, id="tensor-core"), pytest.param(0, 0, id="generic")]
+
+
+@pytest.mark.parametrize("path,expect", PATHS)
+def test_mimo_shaped_small(path, expect):
     spec = small("mimo", layers=SPECS["mimo"].layers[:10], batch=4, seq_kind="uniform",
-                 seq_lo=100, seq_hi=1500, chunk=256, interval=64)
-    run_small(spec, steps=70)          # crosses an eviction interval and page boundaries
+                 seq_lo=100, seq_hi=2500, chunk=256, interval=64)
+    run_small(spec, steps=70, path=path, expect_path=expect)  # crosses eviction and page edges
 
 
-def test_gptoss_shaped_small():
+@pytest.mark.parametrize("path,expect", PATHS)
+def test_gptoss_shaped_small(path, expect):
     spec = small("gptoss", layers=SPECS["gptoss"].layers[:4], batch=6, seq_lo=200, seq_hi=3000,
                  chunk=512, interval=16)
-    run_small(spec, steps=20)
+    run_small(spec, steps=20, path=path, expect_path=expect)
 
 
-def test_llama4_shaped_small_envelope_fp8():
+@pytest.mark.parametrize("path,expect", PATHS)
+def test_llama4_shaped_small_envelope_fp8(path, expect):
     spec = small("llama4", layers=[(CHUNKED, 256, 8), (CHUNKED, 256, 8), (FULL, 0, 8)] * 2,
-                 batch=3, seq_kind="uniform", seq_lo=300, seq_hi=1300, chunk=256, interval=32)
-    run_small(spec, steps=40)
+                 batch=3, seq_kind="uniform", seq_lo=300, seq_hi=2300, chunk=256, interval=32)
+    run_small(spec, steps=40, path=path, expect_path=expect)
+
+
+def test_decode_edge_cases():
+    """Length-1 requests (a single key), requests exactly on page and split
+    boundaries, and a sliding window longer than the prefix."""
+    spec = small("gptoss", layers=[(SLIDING, 127, 8), (FULL, 0, 8)], batch=6,
+                 seq_list=(1, 2, 16, 17, 1024, 1025), chunk=64, interval=16)
+    st = DecodeState(spec, max_steps=4, trace=True, poison_page0=True)
+    st.prefill()
+    st.alloc_decode_buffers()
+    inputs = st.make_decode_inputs(2)
+    for s in range(2):
+        st.decode_step(inputs[s])
+    oa, ort = replay(st)
+    check_state(st, oa, ort)
+    for l in range(2):
+        g = st.outs[l].float().cpu().numpy()
+        q = inputs[-1]["q"][l].float().cpu().numpy()
+        for b in range(st.B):
+            o = oracle_decode(st, oa, ort, l, b, inputs[-1]["seq_h"][b], q[b])
+            assert_close(g[b], o, 2e-2, f"edge layer {l} req {b}")
