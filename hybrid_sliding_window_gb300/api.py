@@ -86,6 +86,9 @@ SIGNATURES = {
     "swa_plan": (I32, [P, I32, P, I64, P, P, P, I32, P, SZ, P]),
     "swa_attn_decode_ws_bytes": (SZ, [P, I32, I32, I32]),
     "swa_attn_decode": (I32, [P, I32, I32, P, I64, P, P, I32, P, P, P, F32, F32, F32, P, P, SZ, P]),
+    "swa_attn_decode_noalloc_max_bytes": (SZ, []),
+    "swa_attn_decode_noalloc": (I32, [P, I32, I32, P, I64, P, P, I32, P, P, P, F32, F32, F32, P,
+                                      P]),
     "swa_attn_extend_ws_bytes": (SZ, [P, I32, I64, I32]),
     "swa_attn_extend": (I32, [P, I32, I32, P, I64, P, P, P, P, I64, I32, I32, P, P, P, F32, F32,
                               F32, P, P, SZ, P]),
@@ -345,6 +348,21 @@ def swa_attn_decode(ctx, layer, req_to_token, req_idx, seq_lens, max_seq_len, pl
                                  _ptr(seq_lens), max_seq_len, _ptr(plan), _ptr(q), _ptr(sinks),
                                  sm_scale, k_scale, v_scale, _ptr(out), _ptr(ws), ws.numel(),
                                  _stream(stream)), ctx.handle)
+
+
+def swa_attn_decode_noalloc_max_bytes():
+    return lib().swa_attn_decode_noalloc_max_bytes()
+
+
+def swa_attn_decode_noalloc(ctx, layer, req_to_token, req_idx, seq_lens, max_seq_len, plan, q,
+                            sinks, sm_scale, out, k_scale=1.0, v_scale=1.0, stream=None):
+    """Decode attention with the library's fixed internal scratch (no workspace)."""
+    bs = seq_lens.numel()
+    stride = req_to_token.shape[1] if req_to_token is not None else 0
+    _check(lib().swa_attn_decode_noalloc(ctx.handle, layer, bs, _ptr(req_to_token), stride,
+                                         _ptr(req_idx), _ptr(seq_lens), max_seq_len, _ptr(plan),
+                                         _ptr(q), _ptr(sinks), sm_scale, k_scale, v_scale,
+                                         _ptr(out), _stream(stream)), ctx.handle)
 
 
 def swa_attn_extend_ws_bytes(ctx, layer, n_tokens, max_seq_len):

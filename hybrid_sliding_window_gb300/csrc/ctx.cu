@@ -178,6 +178,10 @@ swa::PlanView plan_view(const swa_ctx *c, const void *plan, int bs, int max_new)
 
 }  // namespace
 
+void swa::set_ctx_error(swa_ctx *ctx, const char *msg) {
+  if (ctx) ctx->err = msg;
+}
+
 extern "C" {
 
 swa_status swa_pool_sizes(int64_t mem_bytes, int64_t F, int64_t S, int32_t L_full,

@@ -157,6 +157,9 @@ bool tc_extend_supported(const Ctx &c, int layer);
 size_t tc_extend_ws_bytes(const Ctx &c, int layer, int64_t n_tokens, int max_seq_len);
 cudaError_t launch_attn_extend_tc(Ctx &c, const AttnArgs &a, cudaStream_t s);
 
+// Records a message for swa_last_error(ctx) (defined in ctx.cu).
+void set_ctx_error(swa_ctx *ctx, const char *msg);
+
 // Device-side error helper.
 __device__ inline void set_error(int32_t *word, int bits) {
   if (word) atomicOr(word, bits);

@@ -320,6 +320,32 @@ swa_status swa_attn_decode(swa_ctx *ctx, int32_t layer, int32_t bs,
                            float v_scale, void *out, void *ws, size_t ws_bytes,
                            swa_stream_t stream);
 
+/* swa_attn_decode_noalloc: swa_attn_decode for callers that cannot allocate
+ * device memory - engines that give all of HBM to their KV pools at start-up
+ * and allow no later allocation, plug-ins whose host framework exposes no
+ * allocator, and paths where a cudaMalloc (which can synchronise the device)
+ * is not acceptable.  The source pages have no counterpart; it exists for
+ * those callers.  Arguments are swa_attn_decode's without ws / ws_bytes: the
+ * split-KV scratch is a fixed 32 MiB array inside the library
+ * (swa_attn_decode_noalloc_max_bytes()), which every GPU that loads the
+ * library holds until the process exits.  A batch whose scratch
+ * (swa_attn_decode_ws_bytes) exceeds it is rejected with SWA_ERR_INVALID and
+ * a message.  The call allocates nothing: it clears the scratch bytes it
+ * needs (cudaMemsetAsync on `stream`) and runs the same kernels.  The first
+ * call on a device looks up the array's device address, so make that first
+ * call before any stream capture.  All calls on a device share the array and
+ * it keeps the last call's contents; calls that overlap on the GPU (e.g. on
+ * different streams) race on it. */
+size_t swa_attn_decode_noalloc_max_bytes(void);
+swa_status swa_attn_decode_noalloc(swa_ctx *ctx, int32_t layer, int32_t bs,
+                                   const int32_t *req_to_token,
+                                   int64_t rt_stride, const int64_t *req_idx,
+                                   const int64_t *seq_lens, int32_t max_seq_len,
+                                   const void *plan, const void *q,
+                                   const float *sinks, float sm_scale,
+                                   float k_scale, float v_scale, void *out,
+                                   swa_stream_t stream);
+
 /* swa_attn_extend: chunked-prefill queries.  Request b owns query rows
  * qo_indptr[b]..qo_indptr[b+1]-1 (device, bs+1 entries), at positions
  * prefix_lens[b] .. seq_lens[b]-1, causal.  n_tokens = qo_indptr[bs] and
