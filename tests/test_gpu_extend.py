@@ -1,0 +1,61 @@
+"""Chunked-prefill (extend) attention parity: the tcgen05 kernel and the generic
+kernel against the oracle, MiMo-shaped layers (sliding W=128 with 8 KV heads,
+full with 4 KV heads, 64 query heads, D=128, bf16), pages of 16 and 64,
+prefixes that end mid-page, chunks that end mid-tile, an empty prefix, and
+SWA KV evicted below the window before the chunk (evicted slots poisoned)."""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+from hybrid_sliding_window_gb300 import api  # noqa: E402
+from oracle import attention as OT  # noqa: E402
+from tests.harness import Pair, assert_close  # noqa: E402
+
+LAYERS = [(OT.SLIDING, 127, 8), (OT.FULL, 0, 4)]
+
+
+def _run(ps, path, prompt, chunk, layers=LAYERS, chunk0=256):
+    P = Pair(layers, Hq=64, D=128, dtype="bf16", ps=ps, size_full=ps * (4096 // ps + 40),
+             size_swa=ps * (1536 // ps + 40), seed=11, perm_free=True, max_ctx=4096, max_reqs=4)
+    api.swa_set_attn_path(P.ctx, path)
+    rows = [1, 2, 3]
+    lens = np.zeros(3, np.int64)
+    ev = np.zeros(3, np.int64)
+    prompt = np.asarray(prompt, np.int64)
+    while (lens < prompt).any():
+        sel = [i for i in range(3) if lens[i] < prompt[i]]
+        e = ev[sel].copy()
+        P.evict([rows[i] for i in sel], lens[sel], e, 0)
+        ev[sel] = e
+        new = np.minimum(lens[sel] + chunk0, prompt[sel])
+        P.extend([rows[i] for i in sel], lens[sel], new)
+        lens[sel] = new
+    P.evict(rows, lens, ev, 0)
+    seq = lens + np.asarray(chunk, np.int64)
+    P.extend(rows, lens, seq)
+    P.check_state()
+    res = P.extend_attention(rows, lens, seq)
+    return P, res
+
+
+@pytest.mark.parametrize("ps", [16, 64])
+@pytest.mark.parametrize("path,expect", [pytest.param(-1, 2, id="tcgen05"),
+                                         pytest.param(0, 0, id="generic")])
+def test_extend_mimo_shaped(ps, path, expect):
+    P, res = _run(ps, path, prompt=[700, 333, 0], chunk=[150, 77, 40])
+    assert api.swa_last_attn_path(P.ctx) == expect
+    for l, (g, o) in res.items():
+        assert_close(g, o, 2e-2, f"ps={ps} layer {l}")
+    assert api.swa_device_check(P.ctx) == 0
+
+
+def test_extend_long_prefix_many_key_tiles():
+    """Full layer across many 128-key tiles (prefix 2000, chunk 130)."""
+    P, res = _run(64, -1, prompt=[2000, 1290, 5], chunk=[130, 9, 128])
+    assert api.swa_last_attn_path(P.ctx) == 2
+    for l, (g, o) in res.items():
+        assert_close(g, o, 2e-2, f"layer {l}")
