@@ -303,6 +303,85 @@ def run_native(args, rank, world):
     return line
 
 
+def bf16_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+def run_extend(args, rank, world, quiet=False):
+    """Chunked-prefill extend: 4 requests x (24576 prefix + 8192 chunk), MiMo layers."""
+    import numpy as np
+    import torch
+    from hybrid_sliding_window_gb300 import api
+    from hybrid_sliding_window_gb300.workloads import (EXTEND_CHUNK, EXTEND_PREFIX, EXTEND_SPEC,
+                                                       DecodeState, FULL)
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    api.lib()
+    spec = EXTEND_SPEC
+    st = DecodeState(spec, max_steps=EXTEND_CHUNK + 64)
+    st.prefill(prompt=np.full(spec.batch, EXTEND_PREFIX, np.int64), final_evict=False)
+    full_layers = [l for l, (k, _, _) in enumerate(spec.layers) if k == FULL]
+    ev_evict = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    slots_before = st.evicted.copy()
+    r0 = torch.cuda.Event(enable_timing=True)
+    r1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    r0.record()
+    meta = st.extend_round(EXTEND_CHUNK, evict_events=ev_evict)
+    r1.record()
+    torch.cuda.synchronize()
+    round_ms = r0.elapsed_time(r1)
+    evict_ms = ev_evict[0].elapsed_time(ev_evict[1])
+    evicted_slots = int((st.evicted - slots_before).sum())
+    flops = st.extend_flops(meta)
+    # Timed: the attention of the whole chunk round (all 48 layers), repeated.
+    W, K = args.warmup, args.steps
+    for _ in range(W):
+        st.extend_attention(meta)
+    evs = {l: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)] for l in full_layers}
+    clk = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.synchronize()
+    clk.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for k in range(K):
+        st.extend_attention(meta, {l: evs[l][k] for l in full_layers})
+    e1.record()
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    t_ms = e0.elapsed_time(e1) / K
+    full_ms = sum(evs[l][k][0].elapsed_time(evs[l][k][1]) for l in full_layers
+                  for k in range(K)) / (K * len(full_layers))
+    assert api.swa_device_check(st.ctx) == 0
+    burst, sustained, src = bf16_peaks()
+    per_full = flops["full"] / len(full_layers)
+    ach = per_full / (full_ms / 1e3) / 1e12
+    return {
+        "metric": METRIC, "value": round(flops["total"] / (t_ms / 1e3) / 1e12, 2),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(t_ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic",
+        "config": {"workload": spec.description, "flops_per_round": flops["total"],
+                   "l2": "no flush: each round reads ~1.3 GB of KV per full layer pass"},
+        "frac_of_sustained_bf16": round(flops["total"] / (t_ms / 1e3) / 1e12 / sustained, 4),
+        "roofline": {"bound": "tensor", "achieved": round(ach, 1), "peak": burst,
+                     "unit": "TFLOP/s", "frac": round(ach / burst, 4), "traffic": None,
+                     "kernel": "swa_attn_extend on full layers (tcgen05)",
+                     "peak_source": src, "avg_launch_ms": round(full_ms, 3)},
+        "full_round_ms": round(round_ms, 3),
+        "evict": {"slots": evicted_slots, "ms": round(evict_ms, 4),
+                  "slots_per_s": round(evicted_slots / (evict_ms / 1e3), 1)},
+        "clocks": clocks, "attn_path": api.swa_last_attn_path(st.ctx),
+        "gpu_launches": len(spec.layers) * K,
+    }
+
+
 def kernel_hash():
     import hashlib
     h = hashlib.sha256()
@@ -346,7 +425,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="mimo", choices=["mimo", "gptoss", "llama4"])
+    ap.add_argument("--workload", default="mimo", choices=["mimo", "gptoss", "llama4", "extend"])
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--batch", type=int, default=0, help="reduced batch (profiling only)")
@@ -364,6 +443,8 @@ def main():
         tdist.init_process_group("nccl")
     if args.impl == "reference":
         line = run_reference(args, rank, world)
+    elif args.workload == "extend":
+        line = run_extend(args, rank, world)
     else:
         line = run_native(args, rank, world)
     if line is not None:

@@ -79,6 +79,13 @@ class Spec:
         return lb
 
 
+EXTEND_SPEC = Spec("extend", mimo_layers(), 64, 128, "bf16", 64, 4, "fixed", 24577, 24577, 0.8,
+                   128, 3, description="Chunked-prefill extend, MiMo-shaped layers: B=4 requests, "
+                   "24576-token cached prefix + one 8192-token chunk each, W=128, bf16 KV, page 64; "
+                   "SWA KV evicted below the window before the chunk")
+EXTEND_PREFIX = 24576
+EXTEND_CHUNK = 8192
+
 SPECS = {
     "mimo": Spec("mimo", mimo_layers(), 64, 128, "bf16", 64, 64, "uniform", 4096, 32768, 0.8,
                  128, 1, description="MiMo-V2-Flash-shaped decode: 48 layers (39 sliding W=128 "
@@ -222,7 +229,7 @@ class DecodeState:
             api.swa_store_kv(self.ctx, l, k, v, out_f, out_s)
         self.lens[idx] = seq
 
-    def prefill(self, prompt=None):
+    def prefill(self, prompt=None, final_evict=True):
         """Chunked prefill of every request to ``prompt`` (default seq - 1)
         tokens, evicting out-of-window SWA KV before each chunk; requests
         are admitted in groups the SWA pool can hold."""
@@ -237,6 +244,10 @@ class DecodeState:
                 sel = grp[self.lens[grp] < prompt[grp]]
                 self._evict(sel, 0)
                 self._extend(sel, np.minimum(self.lens[sel] + spec.chunk, prompt[sel]))
+            # A finished prompt keeps only its window (what the first decode
+            # step's eviction would leave), so the next group fits.
+            if final_evict:
+                self._evict(grp, 0)
         torch.cuda.synchronize()
 
     # -- decode -----------------------------------------------------------------
@@ -296,6 +307,79 @@ class DecodeState:
             if ev is not None:
                 ev[1].record()
         self.lens = inp["seq_h"].copy()
+
+    # -- extend (one chunked-prefill round) -------------------------------------
+    def extend_round(self, chunk: int, attn_events=None, evict_events=None):
+        """One chunk of every request: eviction before the chunk, alloc_extend,
+        KV store, the per-batch plan and extend attention on every layer.
+        Returns the q tensors, outputs and metadata (kept for parity checks)."""
+        spec = self.spec
+        pre = self.lens.copy()
+        seq = pre + chunk
+        if evict_events:
+            evict_events[0].record()
+        self._evict(np.arange(self.B), 0)
+        if evict_events:
+            evict_events[1].record()
+        self._extend(np.arange(self.B), seq)
+        ext = seq - pre
+        indptr = np.concatenate([[0], np.cumsum(ext)]).astype(np.int64)
+        n = int(indptr[-1])
+        d = lambda x: torch.tensor(x, device=self.dev)
+        meta = dict(pre=pre, seq=seq, indptr=indptr, n=n, pre_d=d(pre), seq_d=d(seq),
+                    indptr_d=d(indptr))
+        plan = torch.zeros(api.swa_plan_bytes(self.ctx, self.B, int(ext.max())), dtype=torch.uint8,
+                           device=self.dev)
+        api.swa_plan(self.ctx, self.rt, self.rows_d, meta["pre_d"], meta["seq_d"], plan,
+                     int(ext.max()))
+        meta["plan"] = plan
+        reqs = torch.tensor(np.repeat(self.rows, ext), device=self.dev)
+        pos = torch.tensor(np.concatenate([np.arange(p, s) for p, s in zip(pre, seq)]),
+                           device=self.dev)
+        meta["q"] = [self._synth(synth.STREAM_Q, l, reqs, pos, spec.Hq)
+                     for l in range(len(spec.layers))]
+        meta["out"] = [torch.empty_like(x) for x in meta["q"]]
+        wsb = max(api.swa_attn_extend_ws_bytes(self.ctx, l, n, int(seq.max()))
+                  for l in range(len(spec.layers)))
+        meta["ws"] = torch.zeros(wsb, dtype=torch.uint8, device=self.dev)
+        self.extend_attention(meta, attn_events)
+        return meta
+
+    def extend_attention(self, meta, attn_events=None):
+        spec = self.spec
+        ext_max = int((meta["seq"] - meta["pre"]).max())
+        for l in range(len(spec.layers)):
+            ev = attn_events.get(l) if attn_events else None
+            if ev is not None:
+                ev[0].record()
+            api.swa_attn_extend(self.ctx, l, self.rt, self.rows_d, meta["pre_d"], meta["seq_d"],
+                                meta["indptr_d"], meta["n"], ext_max, int(meta["seq"].max()),
+                                meta["plan"], meta["q"][l], self.sinks_d[l], self.scale,
+                                meta["out"][l], meta["ws"])
+            if ev is not None:
+                ev[1].record()
+
+    def extend_flops(self, meta) -> dict:
+        """Algorithmic flops of extend attention: 4*D per attended (q-head, key)."""
+        spec = self.spec
+        full = swa = 0
+        for kind, w, hkv in spec.layers:
+            pairs = 0
+            for p0, s in zip(meta["pre"], meta["seq"]):
+                p = np.arange(p0, s)
+                if kind == FULL:
+                    n = p + 1
+                elif kind == SLIDING:
+                    n = p - np.maximum(0, p - w) + 1
+                else:
+                    n = p - (p // w) * w + 1
+                pairs += int(n.sum())
+            f = 4 * spec.D * spec.Hq * pairs
+            if kind == FULL:
+                full += f
+            else:
+                swa += f
+        return {"full": full, "swa": swa, "total": full + swa}
 
     def launches_per_step(self) -> int:
         # evict (3) + alloc_decode (2) + plan (1) + per layer store (1) + attention (1)

@@ -81,9 +81,24 @@ def e4m3_encode_scalar(x: float) -> int:
     return sign | code
 
 
+_BF16_TABLE = []
+
+
+def _bf16_table() -> np.ndarray:
+    """``e4m3_encode_scalar`` of every bf16 value, indexed by its bit pattern."""
+    if not _BF16_TABLE:
+        vals = bf16_decode(np.arange(65536, dtype=np.uint32).astype(np.uint16))
+        _BF16_TABLE.append(np.array([e4m3_encode_scalar(v) for v in vals], dtype=np.uint8))
+    return _BF16_TABLE[0]
+
+
 def e4m3_encode(x, scale: float = 1.0) -> np.ndarray:
     """float values -> E4M3 codes of ``float32(x / scale)``."""
     f = np.asarray(x, dtype=np.float32) / np.float32(scale)
+    bits = bf16_encode(f)
+    if f.size > 4096 and np.array_equal(bf16_decode(bits), f):
+        # Every value is a bf16 value: look the scalar rule up by bit pattern.
+        return _bf16_table()[bits]
     flat = f.reshape(-1)
     out = np.empty(flat.shape, dtype=np.uint8)
     # Encode the distinct values once (inputs are mostly bf16 values).

@@ -254,3 +254,67 @@ def assert_close(gpu, ref, tol, what=""):
         i = np.argwhere(bad)[0]
         raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tol {tol}; first at "
                              f"{tuple(i)}: gpu={gpu[tuple(i)]} ref={ref[tuple(i)]}")
+
+
+# ---------------------------------------------------------------------------
+# Trace replay for workloads built by hybrid_sliding_window_gb300.workloads
+# ---------------------------------------------------------------------------
+from hybrid_sliding_window_gb300.workloads import CHUNKED, FULL, SLIDING  # noqa: E402
+from oracle import codecs as OC  # noqa: E402
+
+OKIND = {FULL: OT.FULL, SLIDING: OT.SLIDING, CHUNKED: OT.CHUNKED}
+
+
+def replay(st: DecodeState):
+    """The oracle allocator driven by the GPU state's recorded calls."""
+    spec = st.spec
+    oa = OA.TwoPoolAllocator(st.size_full, st.size_swa, spec.ps)
+    ort = np.zeros(tuple(st.rt.shape), np.int64)
+    for op in st.trace:
+        if op[0] == "evict":
+            _, rows, pre, ev, interval = op
+            OA.evict_swa(oa, ort, rows, pre, ev, [0] * len(rows), spec.lookback(), interval)
+        else:
+            if op[0] == "extend":
+                _, rows, pre, seq = op
+            else:
+                _, rows, seq = op
+                pre = [s - 1 for s in seq]
+            last = [int(ort[r, p - 1]) if p > 0 else -1 for r, p in zip(rows, pre)]
+            full, _ = oa.alloc_extend(pre, seq, last)
+            off = 0
+            for r, p, s in zip(rows, pre, seq):
+                ort[r, p:s] = full[off:off + s - p]
+                off += s - p
+    return oa, ort
+
+
+def check_state(st, oa, ort):
+    torch.cuda.synchronize()
+    assert api.swa_device_check(st.ctx) == 0
+    np.testing.assert_array_equal(st.ctx.mapping().cpu().numpy(), np.array(oa.mapping, np.int64))
+    for full, led in ((True, oa.full), (False, oa.swa)):
+        free, _ = st.ctx.free_list(full)
+        assert free == led.free
+    np.testing.assert_array_equal(st.rt.cpu().numpy().astype(np.int64), ort)
+    assert api.swa_available_size(st.ctx) == oa.available_size()
+
+
+def oracle_decode(st, oa, ort, layer, b, seq_b, q_row):
+    """Oracle output [Hq, D] for batch entry b at position seq_b - 1."""
+    spec = st.spec
+    kind, w, hkv = spec.layers[layer]
+    p = int(seq_b) - 1
+    row = int(st.rows[b])
+    J = list(OT.key_positions(OKIND[kind], w, p))
+    if kind != FULL:
+        assert all(oa.mapping[int(ort[row, j])] > 0 for j in J), "evicted key in window"
+    bf = spec.dtype != "f32"
+    K = synth.tokens(spec.seed, synth.STREAM_K, layer, [row] * len(J), J, hkv, spec.D, bf16=bf)
+    V = synth.tokens(spec.seed, synth.STREAM_V, layer, [row] * len(J), J, hkv, spec.D, bf16=bf)
+    if spec.dtype == "e4m3":
+        K = OC.e4m3_decode(OC.e4m3_encode(K))
+        V = OC.e4m3_decode(OC.e4m3_encode(V))
+    return OT.attend_heads(q_row.astype(np.float64), K, V, st.sinks_h[layer], st.scale)
+
+
