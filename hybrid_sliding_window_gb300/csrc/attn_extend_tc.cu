@@ -1,27 +1,38 @@
 // Chunked-prefill (extend) attention on the 5th-generation tensor cores
-// (tcgen05 + TMEM), bf16 KV, D = 128, GQA group G in {8, 16}, page size >= 16.
+// (tcgen05 + TMEM + TMA), bf16 KV in the per-layer layout, D = 128, GQA group
+// G in {8, 16}, page size 16..128 (a power of two).
 //
 // Method: "SWA in SGLang" design note - the chunk's queries at positions
 // pre..seq-1 attend causally; sliding layers see the last Wx+1 keys, full
 // layers every earlier key; a per-head sink joins the denominator.
 //
-// GB300 design.  In extend, QK^T and PV are dense tile contractions, so they
-// run on tcgen05.mma (kind::f16, bf16 in, f32 accumulate in tensor memory):
-//   * a CTA owns one 128-row Q tile = (128/G) query tokens x the G query heads
-//     of one KV head (all rows share the KV head's keys);
-//   * keys stream in tiles of 128 rows gathered through the index tables with
-//     cp.async (16-byte chunks, 128-byte swizzle, double buffered);
-//   * one thread issues S = Q K^T (M=128, N=128, K=128) into TMEM columns
-//     0..127 and O += P V into columns 128..255; tcgen05.commit signals an
-//     mbarrier;
-//   * each of the 128 threads owns one TMEM lane = one row: it reads its S
-//     row, applies the causal / window mask, runs the online softmax in
-//     registers, writes its P row (bf16) to shared memory as the A operand of
-//     the next MMA, and rescales its O row in TMEM only when the warp's row
-//     maxima moved.
-// Every wait on an mbarrier has an iteration limit; on expiry the kernel sets
-// an error bit, skips the rest of its work and still releases its TMEM.
+// GB300 design (one CTA per SM, 10 warps, warp-specialised):
+//   * the CTA owns two 128-row Q tiles, each (128/G) consecutive query tokens
+//     x the G query heads of one KV head, so every K/V tile it loads feeds two
+//     QK^T and two PV products;
+//   * warp 9 gathers the Q rows once (cp.async) and then, from one lane,
+//     streams K and V through a two-stage ring with TMA: one 3-D box
+//     {64 dims, 1 head, ps rows} per page and half of D, 128-byte swizzle,
+//     completion counted on "full" mbarriers, slots returned on "empty" ones;
+//   * warp 8 (one lane) issues tcgen05.mma: S_i = Q_i K^T into TMEM columns
+//     [128 i, 128 i + 128) and O_i += P_i V into columns [256 + 128 i, ...),
+//     with P_i read from TMEM where it overwrote S_i, and tcgen05.commit for
+//     every hand-off;
+//   * warps 0-3 and 4-7 are the softmax groups of Q tile 0 and 1: each thread
+//     owns one row (one TMEM lane), reads its S row, masks only the key tiles
+//     that straddle a window or causal edge, and keeps a lazily rescaled
+//     running maximum (O in TMEM is rescaled only when the maximum grew by more
+//     than 2^8), writes P as packed bf16 pairs back to TMEM and signals the
+//     MMA lane; after the last tile it normalises O (with the sink) and stores
+//     its output row.
+// KV pools are zero-initialised by the caller (as the pages' pools are), so
+// rows of a loaded page outside the query's key range hold finite values and
+// their zero softmax weight cancels them exactly; the stage buffers are
+// zeroed once at start for the same reason.
+// Every mbarrier wait has a poll limit; on expiry the kernel sets an error
+// bit, every role leaves its loop, and the TMEM is still released.
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -31,36 +42,35 @@ namespace swa {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kRows = 128;        // Q tile rows (M)
-constexpr int kKeys = 128;        // keys per KV tile (N of QK^T, K of PV)
-constexpr int kThreads = 128;
-constexpr int kTileBytes = kRows * kD * 2;   // one 128 x 128 bf16 tile: 32 KB
-constexpr int kHalf = kTileBytes / 2;        // one 64-column block: 16 KB
-constexpr uint32_t kTmemCols = 256;
-constexpr long kSpinLimit = 1L << 26;        // mbarrier polls before giving up
+constexpr int kRows = 128;                   // rows of one Q tile (M)
+constexpr int kKeys = 128;                   // keys per K/V tile
+constexpr int kThreads = 320;                // 8 softmax warps + MMA warp + load warp
+constexpr int kTileBytes = kRows * kD * 2;   // 128 x 128 bf16 = 32 KB
+constexpr int kHalf = kTileBytes / 2;        // one 64-column block
+constexpr uint32_t kTmemCols = 512;
+constexpr long kSpinLimit = 1L << 24;
+constexpr float kRescaleGap = 8.f;           // log2 units: rescale O when the max grows more
 
 struct TcParams {
   int kind, window, hkv, G, ps, ps_shift;
-  KvAddr addr;
   int64_t pool_rows;
   const int32_t *rt;
   int64_t rt_stride;
   const int64_t *req_idx;
   const int64_t *pre;
-  const int64_t *seq;
   const int64_t *qo_indptr;
   int bs;
-  int qtiles_upper;     // grid.x
+  int items_upper;
   PlanView plan;
   const __nv_bfloat16 *q;
   const float *sinks;
   float scale_log2;
   __nv_bfloat16 *out;
-  int max_pages;        // capacity of the per-CTA page-row table
+  int max_pages;
   int32_t *err;
 };
 
-// ---------------------------------------------------------------- PTX ---
+// ------------------------------------------------------------------ PTX ---
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -68,10 +78,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool p
   int sz = pred ? 16 : 0;
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(sz));
 }
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
-
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
@@ -81,12 +87,22 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
 }
-
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
 }
-// Waits for the phase with the given parity; false when the poll limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}\n" ::"r"(bar),
+      "r"(bytes)
+      : "memory");
+}
+// Bounded wait for the phase of the given parity.  Gives up (returns false)
+// after the poll limit or when another role has already aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
   for (long i = 0; i < kSpinLimit; ++i) {
     uint32_t done;
     asm volatile(
@@ -96,37 +112,48 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
         : "r"(bar), "r"(parity)
         : "memory");
     if (done) return true;
+    if ((i & 1023) == 1023 && *abort_flag) return false;
   }
+  *abort_flag = 1;
   return false;
 }
 
-// Shared-memory matrix descriptor (tcgen05): start >> 4 at [0,14), leading
-// byte offset >> 4 at [16,30), stride byte offset >> 4 at [32,46), version 1
-// at [46,48), layout (2 = 128-byte swizzle) at [61,64).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr >> 4) & 0x3FFF);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
 }
 
-// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (7-9 = 1),
-// B bf16 (10-12 = 1), A K-major (bit 15 = 0), B major at bit 16, N >> 3 at
-// [17,23), M >> 4 at [24,29).
+// tcgen05 shared-memory matrix descriptor: start >> 4 at [0,14), leading byte
+// offset >> 4 at [16,30), stride byte offset >> 4 at [32,46), version 1 at
+// [46,48), layout 2 (128-byte swizzle) at [61,64).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: D f32, A and B bf16, A K-major, B major
+// bit 16, N >> 3 at [17,23), M >> 4 at [24,29).
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+// A operand read from tensor memory (P), B from shared memory (V).
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
 }
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(
@@ -158,8 +185,8 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
-// Byte offset of (row r, 16-byte chunk c in 0..15) inside a 128 x 128 bf16 tile
-// stored as two 64-column blocks of [128 rows][128 B] with the 128-byte swizzle.
+// (row r, 16-byte chunk c in 0..15) of a 128 x 128 bf16 tile stored as two
+// 64-column blocks of [128 rows][128 B] with the 128-byte swizzle.
 __device__ __forceinline__ uint32_t tile_off(int r, int c) {
   return (uint32_t)((c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
@@ -170,71 +197,68 @@ __device__ __forceinline__ int64_t key_lo(int kind, int window, int64_t p) {
   return (p / window) * window;
 }
 
-// Shared memory: [Q 32K][K0 32K][V0 32K][K1 32K][V1 32K][P 32K][page rows][bars]
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kTileBytes;
-constexpr int kOffP = kOffKV + 4 * kTileBytes;
-constexpr int kOffRows = kOffP + kTileBytes;
+// Shared memory (offsets from a 1024-byte aligned base).
+constexpr int kOffQ = 0;                        // Q0, Q1
+constexpr int kOffK = 2 * kTileBytes;           // K stage 0, 1
+constexpr int kOffV = 4 * kTileBytes;           // V stage 0, 1
+constexpr int kOffRows = 6 * kTileBytes;        // int32 page rows [max_pages]
+enum { B_FULLK = 0, B_EMPTYK = 2, B_FULLV = 4, B_EMPTYV = 6, B_SDONE = 8, B_PREADY = 10,
+       B_QFULL = 12, B_ODONE = 13, B_COUNT = 14 };
 
-__global__ void __launch_bounds__(kThreads, 1) k_extend_tc(TcParams P) {
+__global__ void __launch_bounds__(kThreads, 1)
+    k_extend_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                TcParams P) {
   extern __shared__ char smem_raw[];
-  // 1024-byte alignment for the swizzled tiles.
   char *smem = reinterpret_cast<char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const uint32_t sbase = smem_u32(smem);
-  int64_t *s_rows = reinterpret_cast<int64_t *>(smem + kOffRows);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffRows + P.max_pages * 8);
+  const uint32_t sb = smem_u32(smem);
+  int32_t *s_rows = reinterpret_cast<int32_t *>(smem + kOffRows);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffRows + ((P.max_pages * 4 + 7) & ~7));
   __shared__ uint32_t s_tmem;
-  __shared__ int s_abort;
-  __shared__ int64_t s_q0, s_q1, s_pre, s_req;
+  __shared__ volatile int s_abort;
+  __shared__ int64_t s_q0, s_qend, s_pfirst, s_req;
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kvh = blockIdx.y;
   const int G = P.G;
-  const int T = kRows / G;                       // query tokens per tile
+  const int T = kRows / G;                 // tokens per Q tile
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
-  // ---- which Q tile: longest (latest) tiles first ----
+  // ---- work item: two Q tiles of one request, latest first ----
   if (tid == 0) {
-    int64_t tau = (int64_t)P.qtiles_upper - 1 - blockIdx.x;
-    int64_t acc = 0;
+    int64_t tau = (int64_t)P.items_upper - 1 - blockIdx.x, acc = 0;
     s_req = -1;
     for (int b = 0; b < P.bs; ++b) {
       const int64_t ext = P.qo_indptr[b + 1] - P.qo_indptr[b];
-      const int64_t nt = (ext + T - 1) / T;
-      if (tau < acc + nt) {
-        const int64_t local = (tau - acc) * T;
+      const int64_t n = (ext + 2 * T - 1) / (2 * T);
+      if (tau < acc + n) {
+        const int64_t local = (tau - acc) * 2 * T;
         s_req = b;
         s_q0 = P.qo_indptr[b] + local;
-        s_q1 = min(P.qo_indptr[b + 1], s_q0 + T);
-        s_pre = P.pre[b] + local;                 // position of the tile's first query
+        s_qend = P.qo_indptr[b + 1];
+        s_pfirst = P.pre[b] + local;
         break;
       }
-      acc += nt;
+      acc += n;
     }
     s_abort = 0;
   }
   __syncthreads();
   if (s_req < 0) return;
   const int b = (int)s_req;
-  const int64_t q0 = s_q0, nq = s_q1 - s_q0, p_first = s_pre;
-  const int64_t p_last = p_first + nq - 1;
-
-  // Row of this thread: token tr, head g.
-  const int r = tid;
-  const int tr = r / G, g = r % G;
-  const bool row_valid = tr < nq;
-  const int64_t p_row = p_first + tr;
-  const int64_t lo_row = key_lo(P.kind, P.window, p_row);
-
-  // Key range of the tile.
+  const int64_t q0 = s_q0, n_tok = min((int64_t)2 * T, s_qend - s_q0);
+  const int64_t p_first = s_pfirst, p_last = p_first + n_tok - 1;
   const int64_t k_lo = key_lo(P.kind, P.window, p_first);
   const int64_t k_hi = p_last;
-  const int n_tiles = (int)((k_hi - k_lo + kKeys) / kKeys);
-  if (k_hi / P.ps - k_lo / P.ps + 1 > P.max_pages) {   // max_seq_len was too small
+  const int64_t kt0 = (k_lo / kKeys) * kKeys;      // key tiles are 128-aligned
+  const int n_tiles = (int)((k_hi - kt0) / kKeys + 1);
+  const int64_t pg0 = kt0 / P.ps;
+  const int n_pg = (int)(k_hi / P.ps - pg0 + 1);
+  if (n_pg > P.max_pages) {
     if (tid == 0) set_error(P.err, SWA_DEVERR_RANGE);
     return;
   }
 
-  // ---- TMEM ----
+  // ---- set-up: TMEM, barriers, page rows, zeroed K/V stages ----
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
                      smem_u32(&s_tmem)),
@@ -242,218 +266,250 @@ __global__ void __launch_bounds__(kThreads, 1) k_extend_tc(TcParams P) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::);
   }
   if (tid == 0) {
-    mbar_init(smem_u32(&bars[0]), 1);
-    mbar_init(smem_u32(&bars[1]), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_FULLK + i), 1);
+      mbar_init(bar(B_EMPTYK + i), 1);
+      mbar_init(bar(B_FULLV + i), 1);
+      mbar_init(bar(B_EMPTYV + i), 1);
+      mbar_init(bar(B_SDONE + i), 1);
+      mbar_init(bar(B_PREADY + i), kRows);
+    }
+    mbar_init(bar(B_QFULL), 32);
+    mbar_init(bar(B_ODONE), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
-  // ---- page rows of the key range ----
-  const int64_t pg0 = k_lo / P.ps;
-  const int n_pg = (int)(k_hi / P.ps - pg0 + 1);
-  const int64_t page_stride = (int64_t)P.ps * (P.addr.blocks ? P.addr.blocks : 1);
   const int64_t max_page = P.pool_rows / P.ps - 1;
   for (int i = tid; i < n_pg; i += kThreads) {
-    const int64_t pos = (pg0 + i) * P.ps > k_lo ? (pg0 + i) * P.ps : k_lo;
-    int64_t page;
-    if (P.kind == SWA_LAYER_FULL) {
-      page = P.rt[P.req_idx[b] * P.rt_stride + pos] / P.ps;
-    } else {
-      const int32_t *h = P.plan.hdr + b * 4;
-      const int64_t k = pos / P.ps - h[2];
-      page = (pos >= h[0] && k >= 0 && k < h[3]) ? P.plan.pages[(int64_t)b * P.plan.max_pages + k] : -1;
-      if (page == 0) set_error(P.err, SWA_DEVERR_WINDOW_EVICTED);
+    const int64_t pos0 = (pg0 + i) * P.ps;
+    const int64_t pos = pos0 > k_lo ? pos0 : k_lo;
+    int64_t page = -2;                       // -2: not loaded (outside the key range)
+    if (pos <= k_hi && pos0 + P.ps > k_lo) {
+      if (P.kind == SWA_LAYER_FULL) {
+        page = P.rt[P.req_idx[b] * P.rt_stride + pos] / P.ps;
+      } else {
+        const int32_t *h = P.plan.hdr + b * 4;
+        const int64_t k = pos / P.ps - h[2];
+        page = (pos >= h[0] && k >= 0 && k < h[3]) ? P.plan.pages[(int64_t)b * P.plan.max_pages + k]
+                                                   : -1;
+        if (page == 0) set_error(P.err, SWA_DEVERR_WINDOW_EVICTED);
+      }
+      if (page < 0 || page > max_page) {
+        set_error(P.err, SWA_DEVERR_RANGE);
+        page = 0;
+      }
     }
-    if (page < 0 || page > max_page) {
-      set_error(P.err, SWA_DEVERR_RANGE);
-      page = 0;
-    }
-    s_rows[i] = page * page_stride;
+    s_rows[i] = page == -2 ? -1 : (int32_t)(page * P.ps);
   }
-  // ---- Q tile ----
-  const int Hq = P.hkv * G;
-  for (int i = tid; i < kRows * 16; i += kThreads) {
-    const int rr = i >> 4, c = i & 15;
-    const int t2 = rr / G, g2 = rr % G;
-    const bool ok = t2 < nq;
-    const __nv_bfloat16 *src = P.q + ((q0 + (ok ? t2 : 0)) * Hq + kvh * G + g2) * kD + c * 8;
-    cp_async16(sbase + kOffQ + tile_off(rr, c), src, ok);
-  }
-  __syncthreads();   // page rows, barriers, TMEM address visible
+  for (int i = tid; i < 4 * kTileBytes / 16; i += kThreads)
+    reinterpret_cast<uint4 *>(smem + kOffK)[i] = make_uint4(0, 0, 0, 0);
+  fence_async_smem();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const uint32_t tS = tmem, tO = tmem + 128;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-
-  const char *kb = P.addr.k + (int64_t)kvh * kD * 2;
-  const char *vb = P.addr.v + (int64_t)kvh * kD * 2;
-  auto load_kv = [&](int t) {
-    const uint32_t dk = sbase + kOffKV + (t & 1) * 2 * kTileBytes;
-    const uint32_t dv = dk + kTileBytes;
-    const int64_t j0 = k_lo + (int64_t)t * kKeys;
-    for (int i = tid; i < kKeys * 16; i += kThreads) {
-      const int rr = i >> 4, c = i & 15;
-      const int64_t j = j0 + rr;
-      const bool ok = j <= k_hi;
-      int64_t off = 0;
-      if (ok) {
-        int64_t pg, in;
-        if (P.ps_shift >= 0) {
-          pg = j >> P.ps_shift;
-          in = j & ((1 << P.ps_shift) - 1);
-        } else {
-          pg = j / P.ps;
-          in = j % P.ps;
-        }
-        off = (s_rows[pg - pg0] + in) * P.addr.row_bytes + c * 16;
-      }
-      cp_async16(dk + tile_off(rr, c), kb + off, ok);
-      cp_async16(dv + tile_off(rr, c), vb + off, ok);
-    }
-  };
-
-  load_kv(0);
-  cp_commit();
-
   constexpr uint32_t kIdS = idesc_f16(128, 128, false);
   constexpr uint32_t kIdO = idesc_f16(128, 128, true);
-  float m_run = -INFINITY, l_run = 0.f;
-  uint32_t phase_s = 0, phase_o = 0;
-  bool o_init = false;
 
-  for (int t = 0; t < n_tiles; ++t) {
-    if (t + 1 < n_tiles) load_kv(t + 1);
-    cp_commit();
-    cp_wait<1>();
+  if (warp == 9) {
+    // ===================== producer: Q gather, then K/V pages =====================
+    const int Hq = P.hkv * G;
+    for (int i = lane; i < 2 * kRows * 16; i += 32) {
+      const int qt = i / (kRows * 16), rr = (i / 16) % kRows, c = i % 16;
+      const int64_t tok = q0 + qt * T + rr / G;
+      const bool ok = tok < s_qend && (qt * T + rr / G) < n_tok;
+      const __nv_bfloat16 *src = P.q + ((ok ? tok : q0) * Hq + kvh * G + rr % G) * kD + c * 8;
+      cp_async16(sb + kOffQ + qt * kTileBytes + tile_off(rr, c), src, ok);
+    }
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
     fence_async_smem();
-    __syncthreads();
-    if (s_abort) break;
-    const uint32_t kt = sbase + kOffKV + (t & 1) * 2 * kTileBytes;
-    const uint32_t vt = kt + kTileBytes;
-    // ---- S = Q K^T ----
-    if (tid == 0) {
+    mbar_arrive(bar(B_QFULL));
+    if (lane == 0) {
+      const int pages_per_tile = kKeys / P.ps;
+      for (int t = 0; t < n_tiles && !s_abort; ++t) {
+        const int s = t & 1;
+        for (int kv = 0; kv < 2; ++kv) {
+          if (t >= 2 && !mbar_wait(bar((kv ? B_EMPTYV : B_EMPTYK) + s), ((t >> 1) - 1) & 1, &s_abort))
+            break;
+          uint32_t bytes = 0;
+          for (int i = 0; i < pages_per_tile; ++i) {
+            const int pi = t * pages_per_tile + i;
+            if (pi < n_pg && s_rows[pi] >= 0) bytes += (uint32_t)P.ps * 256;
+          }
+          const uint32_t full = bar((kv ? B_FULLV : B_FULLK) + s);
+          mbar_expect_tx(full, bytes);
+          const uint32_t dst = sb + (kv ? kOffV : kOffK) + s * kTileBytes;
+          for (int i = 0; i < pages_per_tile; ++i) {
+            const int pi = t * pages_per_tile + i;
+            if (pi >= n_pg || s_rows[pi] < 0) continue;
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(dst + h * kHalf + i * P.ps * 128, kv ? &tmV : &tmK, h * 64, kvh,
+                          s_rows[pi], full);
+          }
+        }
+      }
+    }
+  } else if (warp == 8) {
+    // ===================== MMA issue (one lane) =====================
+    if (lane == 0 && mbar_wait(bar(B_QFULL), 0, &s_abort)) {
       tc_fence_after();
+      for (int t = 0; t < n_tiles; ++t) {
+        const int s = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
+        if (!mbar_wait(bar(B_FULLK + s), ph, &s_abort)) break;
+        tc_fence_after();
+        const uint32_t kt = sb + kOffK + s * kTileBytes;
+        for (int i = 0; i < 2; ++i) {
+          const uint32_t qa = sb + kOffQ + i * kTileBytes;
 #pragma unroll
-      for (int ks = 0; ks < kD / 16; ++ks) {
-        const uint32_t koff = (ks >> 2) * kHalf + (ks & 3) * 32;
-        tc_mma(tS, smem_desc(sbase + kOffQ + koff, 16, 1024), smem_desc(kt + koff, 16, 1024), kIdS,
-               ks > 0);
+          for (int ks = 0; ks < kD / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
+            mma_ss(tmem + i * 128, smem_desc(qa + off, 16, 1024), smem_desc(kt + off, 16, 1024), kIdS,
+                   ks > 0);
+          }
+          tc_commit(bar(B_SDONE + i));
+        }
+        tc_commit(bar(B_EMPTYK + s));
+        if (!mbar_wait(bar(B_FULLV + s), ph, &s_abort)) break;
+        const uint32_t vt = sb + kOffV + s * kTileBytes;
+        bool ok = true;
+        for (int i = 0; i < 2; ++i) {
+          if (!mbar_wait(bar(B_PREADY + i), t & 1, &s_abort)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < kKeys / 16; ++ks)
+            mma_ts(tmem + 256 + i * 128, tmem + i * 128 + ks * 8,
+                   smem_desc(vt + ks * 16 * 128, kHalf, 1024), kIdO, (t > 0 || ks > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
+        tc_commit(bar(B_EMPTYV + s));
       }
-      tc_commit(smem_u32(&bars[0]));
+      tc_commit(bar(B_ODONE));
     }
-    if (!mbar_wait(smem_u32(&bars[0]), phase_s)) {
-      set_error(P.err, SWA_DEVERR_RANGE);
-      s_abort = 1;
-    }
-    phase_s ^= 1;
-    tc_fence_after();
-    // ---- softmax on this thread's row ----
-    const int64_t j0 = k_lo + (int64_t)t * kKeys;
-    float s[kKeys];
-#pragma unroll
-    for (int cb = 0; cb < kKeys / 32; ++cb) {
-      uint32_t rr[32];
-      TC_LD32(tS + lane_base + cb * 32, rr);
-      tc_wait_ld();
-#pragma unroll
-      for (int e = 0; e < 32; ++e) s[cb * 32 + e] = __uint_as_float(rr[e]);
-    }
-    float mx = -INFINITY;
-#pragma unroll
-    for (int e = 0; e < kKeys; ++e) {
-      const int64_t j = j0 + e;
-      float v = s[e] * P.scale_log2;
-      if (!row_valid || j < lo_row || j > p_row) v = -INFINITY;
-      s[e] = v;
-      mx = fmaxf(mx, v);
-    }
-    const float m_new = fmaxf(m_run, mx);
-    const float mu = m_new == -INFINITY ? 0.f : m_new;
-    const float corr = exp2f(m_run - mu);
-    float psum = 0.f;
-    char *prow = smem + kOffP;
-#pragma unroll
-    for (int c = 0; c < kKeys / 8; ++c) {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float a0 = exp2f(s[c * 8 + 2 * e] - mu);
-        const float a1 = exp2f(s[c * 8 + 2 * e + 1] - mu);
-        __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
-        psum += __low2float(h) + __high2float(h);
-        w[e] = *reinterpret_cast<uint32_t *>(&h);
+  } else {
+    // ===================== softmax group i (warps 4i .. 4i+3) =====================
+    const int grp = warp >> 2;
+    const int r = tid & 127;                    // row of Q tile grp = TMEM lane
+    const int tr = grp * T + r / G, g = r % G;  // token offset in the item, head
+    const bool row_valid = tr < n_tok;
+    const int64_t p_row = p_first + tr;
+    const int64_t lo_row = key_lo(P.kind, P.window, p_row);
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + grp * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + grp * 128 + lane_off;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool alive = true;
+    for (int t = 0; t < n_tiles; ++t) {
+      // Warp-uniform outcome: the TMEM loads below are warp-collective.
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_SDONE + grp), t & 1, &s_abort))) {
+        alive = false;
+        break;
       }
-      *reinterpret_cast<uint4 *>(prow + tile_off(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+      tc_fence_after();
+      const int64_t j0 = kt0 + (int64_t)t * kKeys;
+      const bool edge = !row_valid || j0 < lo_row || j0 + kKeys - 1 > p_row;
+      // Key e of this tile counts iff lo_row <= j0 + e <= p_row (edge tiles only).
+      const int e_lo = edge ? (int)max((int64_t)0, min((int64_t)kKeys, lo_row - j0)) : 0;
+      const int e_hi = edge ? (row_valid ? (int)max((int64_t)-1, min((int64_t)kKeys - 1, p_row - j0))
+                                         : -1)
+                            : kKeys - 1;
+      // Pass 1: row maximum (S is read from TMEM twice instead of held in registers).
+      float mx = -INFINITY;
+#pragma unroll
+      for (int cb = 0; cb < kKeys / 32; ++cb) {
+        uint32_t rr[32];
+        TC_LD32(tS + cb * 32, rr);
+        tc_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int ee = cb * 32 + e;
+          if (ee >= e_lo && ee <= e_hi) mx = fmaxf(mx, __uint_as_float(rr[e]));
+        }
+      }
+      mx = mx == -INFINITY ? -INFINITY : mx * P.scale_log2;
+      // Lazy rescale: move the reference maximum only when it grows by more
+      // than kRescaleGap (weights stay below 2^kRescaleGap meanwhile).
+      float corr = 1.f;
+      if (mx > m_run + kRescaleGap || (m_run == -INFINITY && mx != -INFINITY)) {
+        corr = m_run == -INFINITY ? 0.f : exp2f(m_run - mx);
+        m_run = mx;
+      }
+      if (t > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll
+        for (int cb = 0; cb < kD / 32; ++cb) {
+          uint32_t rr[32];
+          TC_LD32(tO + cb * 32, rr);
+          tc_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * corr);
+          TC_ST32(tO + cb * 32, rr);
+        }
+      }
+      l_run *= corr;
+      const float mu = m_run == -INFINITY ? 0.f : m_run;
+      const float sc = P.scale_log2;
+      // Pass 2: P = exp2(scale*s - m) as packed bf16 pairs, written over the S
+      // columns already consumed (64-key half cb -> columns [32 cb, 32 cb + 32)).
+      float psum = 0.f;
+#pragma unroll
+      for (int cb = 0; cb < 2; ++cb) {
+        uint32_t lo[32], hi[32];
+        TC_LD32(tS + cb * 64, lo);
+        TC_LD32(tS + cb * 64 + 32, hi);
+        tc_wait_ld();
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const uint32_t x0 = e < 16 ? lo[2 * e] : hi[2 * e - 32];
+          const uint32_t x1 = e < 16 ? lo[2 * e + 1] : hi[2 * e - 31];
+          const int k0 = cb * 64 + 2 * e;
+          float a0 = exp2f(fmaf(__uint_as_float(x0), sc, -mu));
+          float a1 = exp2f(fmaf(__uint_as_float(x1), sc, -mu));
+          if (k0 < e_lo || k0 > e_hi) a0 = 0.f;
+          if (k0 + 1 < e_lo || k0 + 1 > e_hi) a1 = 0.f;
+          __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
+          psum += __low2float(h) + __high2float(h);
+          pk[e] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        TC_ST32(tS + cb * 32, pk);
+      }
+      l_run += psum;
+      tc_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(B_PREADY + grp));
     }
-    l_run = l_run * corr + psum;
-    m_run = m_new;
-    // Rescale this warp's O rows unless no row maximum moved.
-    if (o_init && __any_sync(0xffffffffu, corr != 1.f)) {
+    // ---- epilogue ----
+    if (alive && __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), 0, &s_abort))) {
+      tc_fence_after();
+      float sg2 = -INFINITY;
+      if (P.sinks) sg2 = P.sinks[kvh * G + g] * 1.4426950408889634f;
+      const float mr = m_run == -INFINITY ? 0.f : m_run;
+      const float mfin = fmaxf(mr, sg2);
+      const float rsc = exp2f(mr - mfin);
+      const float denom = l_run * rsc + (P.sinks ? exp2f(sg2 - mfin) : 0.f);
+      const float f = denom > 0.f ? rsc / denom : 0.f;
+      const int Hq = P.hkv * G;
+      __nv_bfloat16 *orow = P.out + ((q0 + (row_valid ? tr : 0)) * Hq + kvh * G + g) * kD;
 #pragma unroll
       for (int cb = 0; cb < kD / 32; ++cb) {
         uint32_t rr[32];
-        TC_LD32(tO + lane_base + cb * 32, rr);
+        TC_LD32(tO + cb * 32, rr);
         tc_wait_ld();
+        if (row_valid) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * corr);
-        TC_ST32(tO + lane_base + cb * 32, rr);
-      }
-      tc_wait_st();
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    // ---- O += P V ----
-    if (tid == 0) {
-      tc_fence_after();
+          for (int e = 0; e < 32; e += 8) {
+            uint32_t w[4];
 #pragma unroll
-      for (int ks = 0; ks < kKeys / 16; ++ks) {
-        const uint32_t aoff = (ks >> 2) * kHalf + (ks & 3) * 32;
-        // V as an MN-major operand: 16 keys = 2 swizzle atoms of 8 rows (1024 B
-        // apart); the two 64-column blocks of D are 16 KB apart.
-        tc_mma(tO, smem_desc(sbase + kOffP + aoff, 16, 1024),
-               smem_desc(vt + ks * 16 * 128, kHalf, 1024), kIdO, (o_init || ks > 0) ? 1u : 0u);
-      }
-      tc_commit(smem_u32(&bars[1]));
-    }
-    if (!mbar_wait(smem_u32(&bars[1]), phase_o)) {
-      set_error(P.err, SWA_DEVERR_RANGE);
-      s_abort = 1;
-    }
-    phase_o ^= 1;
-    tc_fence_after();
-    o_init = true;
-  }
-  cp_wait<0>();
-  __syncthreads();
-
-  // ---- epilogue: O / (l + sink) ----
-  if (!s_abort && o_init) {
-    float sg2 = -INFINITY;
-    if (P.sinks) sg2 = P.sinks[kvh * G + g] * 1.4426950408889634f;
-    const float mfin = fmaxf(m_run == -INFINITY ? 0.f : m_run, sg2);
-    const float rsc = exp2f((m_run == -INFINITY ? 0.f : m_run) - mfin);
-    const float denom = l_run * rsc + (P.sinks ? exp2f(sg2 - mfin) : 0.f);
-    const float f = denom > 0.f ? rsc / denom : 0.f;
-    __nv_bfloat16 *orow = P.out + ((q0 + (row_valid ? tr : 0)) * Hq + kvh * G + g) * kD;
-#pragma unroll
-    for (int cb = 0; cb < kD / 32; ++cb) {
-      uint32_t rr[32];
-      TC_LD32(tO + lane_base + cb * 32, rr);
-      tc_wait_ld();
-      if (row_valid) {
-#pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          uint32_t w[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(rr[e + 2 * k]) * f,
-                                                     __uint_as_float(rr[e + 2 * k + 1]) * f);
-            w[k] = *reinterpret_cast<uint32_t *>(&h);
+            for (int k = 0; k < 4; ++k) {
+              __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(rr[e + 2 * k]) * f,
+                                                       __uint_as_float(rr[e + 2 * k + 1]) * f);
+              w[k] = *reinterpret_cast<uint32_t *>(&h);
+            }
+            *reinterpret_cast<uint4 *>(orow + cb * 32 + e) = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          *reinterpret_cast<uint4 *>(orow + cb * 32 + e) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
     }
   }
+  if (s_abort && tid == 0) set_error(P.err, SWA_DEVERR_RANGE);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -462,15 +518,50 @@ __global__ void __launch_bounds__(kThreads, 1) k_extend_tc(TcParams P) {
   }
 }
 
-int tc_max_pages(const Ctx &c, int max_seq_len) {
-  return max_seq_len / c.cfg.page_size + 3;
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
 }
+
+bool ps_ok(int ps) { return ps >= 16 && ps <= 128 && (ps & (ps - 1)) == 0; }
 
 }  // namespace
 
+void make_kv_tensor_maps(Ctx &c, int layer) {
+  LayerInfo &L = c.layers[layer];
+  L.tma = false;
+  if (c.cfg.layout != SWA_LAYOUT_PER_LAYER || c.cfg.kv_dtype != SWA_DTYPE_BF16 ||
+      c.cfg.head_dim != kD || !ps_ok(c.cfg.page_size))
+    return;
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return;
+  const int64_t rows = (L.in_full ? c.cfg.size_full : c.cfg.size_swa) + c.cfg.page_size;
+  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)L.hkv, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)L.hkv * kD * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)c.cfg.page_size};
+  cuuint32_t estr[3] = {1, 1, 1};
+  for (int kv = 0; kv < 2; ++kv) {
+    CUresult r = fn(kv ? &L.tmv : &L.tmk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    kv ? (void *)L.addr.v : (void *)L.addr.k, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return;
+  }
+  L.tma = true;
+}
+
 bool tc_extend_supported(const Ctx &c, int layer) {
-  if (c.cfg.kv_dtype != SWA_DTYPE_BF16 || c.cfg.head_dim != kD) return false;
-  if (c.cfg.page_size < 16) return false;
+  if (!c.layers[layer].tma) return false;
   const int G = c.cfg.num_q_heads / c.layers[layer].hkv;
   return G == 8 || G == 16;
 }
@@ -486,32 +577,30 @@ cudaError_t launch_attn_extend_tc(Ctx &c, const AttnArgs &a, cudaStream_t s) {
   P.hkv = L.hkv;
   P.G = c.cfg.num_q_heads / L.hkv;
   P.ps = c.cfg.page_size;
-  P.ps_shift = (P.ps & (P.ps - 1)) == 0 ? __builtin_ctz((unsigned)P.ps) : -1;
-  P.addr = L.addr;
+  P.ps_shift = __builtin_ctz((unsigned)P.ps);
   P.pool_rows = (L.in_full ? c.cfg.size_full : c.cfg.size_swa) + c.cfg.page_size;
   P.rt = a.rt;
   P.rt_stride = a.rt_stride;
   P.req_idx = a.req_idx;
   P.pre = a.pre;
-  P.seq = a.seq;
   P.qo_indptr = a.qo_indptr;
   P.bs = a.bs;
-  const int T = kRows / P.G;
-  P.qtiles_upper = (int)((a.nq + T - 1) / T + a.bs);
+  const int T2 = 2 * (kRows / P.G);
+  P.items_upper = (int)((a.nq + T2 - 1) / T2 + a.bs);
   P.plan = a.plan;
   P.q = static_cast<const __nv_bfloat16 *>(a.q);
   P.sinks = a.sinks;
   P.scale_log2 = a.scale * 1.4426950408889634f;
   P.out = static_cast<__nv_bfloat16 *>(a.out);
-  P.max_pages = tc_max_pages(c, a.max_seq_len);
+  P.max_pages = a.max_seq_len / P.ps + kKeys / P.ps + 2;
   P.err = c.err_word;
-  const size_t smem = 1024 + kOffRows + (size_t)P.max_pages * 8 + 64;
+  const size_t smem = 1024 + kOffRows + ((size_t)P.max_pages * 4 + 7) / 8 * 8 + B_COUNT * 8;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(k_extend_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(k_extend_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(P.qtiles_upper, L.hkv);
-  k_extend_tc<<<grid, kThreads, smem, s>>>(P);
+  dim3 grid(P.items_upper, L.hkv);
+  k_extend_tc<<<grid, kThreads, smem, s>>>(L.tmk, L.tmv, P);
   return cudaGetLastError();
 }
 

@@ -249,6 +249,7 @@ swa_status swa_ctx_create(const swa_config *cfg, void *state_dev, const int64_t 
                         c->counters + SWA_CTR_SWA_HEAD, c->counters + SWA_CTR_SWA_COUNT,
                         c->counters + SWA_CTR_SWA_STAGED, c->np_swa};
   c->err_word = reinterpret_cast<int32_t *>(c->counters + SWA_CTR_ERROR);
+  for (int l = 0; l < cfg->num_layers; ++l) swa::make_kv_tensor_maps(*c, l);
   c->h_count_full = c->np_full;
   c->h_count_swa = c->np_swa;
   e = swa::launch_init_state(*c, init_free_full, init_free_swa, (cudaStream_t)stream);

@@ -1,6 +1,7 @@
 // Internal declarations shared by the libswa translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -46,6 +47,8 @@ struct LayerInfo {
   int pool_layer;
   bool in_full;
   KvAddr addr;
+  bool tma = false;       // TMA tensor maps below are valid
+  CUtensorMap tmk, tmv;   // per-layer K / V as [rows][Hkv][D], box {64, 1, ps}
 };
 
 // Batch scratch in the state blob used by the eviction pass.
@@ -154,6 +157,9 @@ size_t mma_decode_ws_bytes(const Ctx &c, int layer, int64_t nq, int max_seq_len)
 cudaError_t launch_attn_decode_mma(Ctx &c, const AttnArgs &a, cudaStream_t s);
 
 bool tc_extend_supported(const Ctx &c, int layer);
+// Builds the TMA tensor maps of one layer (bf16, D = 128, per-layer layout);
+// leaves tma = false when the layer does not qualify or encoding fails.
+void make_kv_tensor_maps(Ctx &c, int layer);
 size_t tc_extend_ws_bytes(const Ctx &c, int layer, int64_t n_tokens, int max_seq_len);
 cudaError_t launch_attn_extend_tc(Ctx &c, const AttnArgs &a, cudaStream_t s);
 
