@@ -322,6 +322,11 @@ def run_extend(args, rank, world, quiet=False):
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     api.lib()
     spec = EXTEND_SPEC
+    if args.layers:
+        # Reduced layer count for profiler captures only (named in the config line).
+        import dataclasses
+        spec = dataclasses.replace(spec, layers=spec.layers[:args.layers],
+                                   description=spec.description + f" [reduced: layers={args.layers}]")
     st = DecodeState(spec, max_steps=EXTEND_CHUNK + 64)
     st.prefill(prompt=np.full(spec.batch, EXTEND_PREFIX, np.int64), final_evict=False)
     full_layers = [l for l, (k, _, _) in enumerate(spec.layers) if k == FULL]

@@ -183,6 +183,13 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
         "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]))
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+// The SFU's base-2 exponential (flushes denormal results to zero, which only
+// affects weights below 2^-126 relative to the row maximum).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
 // (row r, 16-byte chunk c in 0..15) of a 128 x 128 bf16 tile stored as two
@@ -349,41 +356,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 8) {
     // ===================== MMA issue (one lane) =====================
-    if (lane == 0 && mbar_wait(bar(B_QFULL), 0, &s_abort)) {
-      tc_fence_after();
-      for (int t = 0; t < n_tiles; ++t) {
-        const int s = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
-        if (!mbar_wait(bar(B_FULLK + s), ph, &s_abort)) break;
-        tc_fence_after();
-        const uint32_t kt = sb + kOffK + s * kTileBytes;
-        for (int i = 0; i < 2; ++i) {
-          const uint32_t qa = sb + kOffQ + i * kTileBytes;
+    // Order per tile t: O0(t), S0(t+1), O1(t), S1(t+1) - softmax group 0 works
+    // on tile t+1 while the tensor core runs O1(t) and S1(t+1), and group 1
+    // likewise one slot later.
+    auto issue_s = [&](int i, int t) {
+      const uint32_t qa = sb + kOffQ + i * kTileBytes;
+      const uint32_t kt = sb + kOffK + (t & 1) * kTileBytes;
 #pragma unroll
-          for (int ks = 0; ks < kD / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
-            mma_ss(tmem + i * 128, smem_desc(qa + off, 16, 1024), smem_desc(kt + off, 16, 1024), kIdS,
-                   ks > 0);
-          }
-          tc_commit(bar(B_SDONE + i));
-        }
-        tc_commit(bar(B_EMPTYK + s));
-        if (!mbar_wait(bar(B_FULLV + s), ph, &s_abort)) break;
-        const uint32_t vt = sb + kOffV + s * kTileBytes;
-        bool ok = true;
-        for (int i = 0; i < 2; ++i) {
-          if (!mbar_wait(bar(B_PREADY + i), t & 1, &s_abort)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < kKeys / 16; ++ks)
-            mma_ts(tmem + 256 + i * 128, tmem + i * 128 + ks * 8,
-                   smem_desc(vt + ks * 16 * 128, kHalf, 1024), kIdO, (t > 0 || ks > 0) ? 1u : 0u);
-        }
-        if (!ok) break;
-        tc_commit(bar(B_EMPTYV + s));
+      for (int ks = 0; ks < kD / 16; ++ks) {
+        const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
+        mma_ss(tmem + i * 128, smem_desc(qa + off, 16, 1024), smem_desc(kt + off, 16, 1024), kIdS,
+               ks > 0);
       }
-      tc_commit(bar(B_ODONE));
+      tc_commit(bar(B_SDONE + i));
+    };
+    auto issue_o = [&](int i, int t) {
+      const uint32_t vt = sb + kOffV + (t & 1) * kTileBytes;
+#pragma unroll
+      for (int ks = 0; ks < kKeys / 16; ++ks)
+        mma_ts(tmem + 256 + i * 128, tmem + i * 128 + ks * 8,
+               smem_desc(vt + ks * 16 * 128, kHalf, 1024), kIdO, (t > 0 || ks > 0) ? 1u : 0u);
+    };
+    if (lane == 0 && mbar_wait(bar(B_QFULL), 0, &s_abort) &&
+        mbar_wait(bar(B_FULLK + 0), 0, &s_abort)) {
+      tc_fence_after();
+      issue_s(0, 0);
+      issue_s(1, 0);
+      tc_commit(bar(B_EMPTYK + 0));
+      for (int t = 0; t < n_tiles; ++t) {
+        const int s = t & 1, s1 = (t + 1) & 1;
+        const bool more = t + 1 < n_tiles;
+        if (!mbar_wait(bar(B_FULLV + s), (t >> 1) & 1, &s_abort)) break;
+        if (!mbar_wait(bar(B_PREADY + 0), t & 1, &s_abort)) break;
+        tc_fence_after();
+        issue_o(0, t);
+        if (more) {
+          if (!mbar_wait(bar(B_FULLK + s1), ((t + 1) >> 1) & 1, &s_abort)) break;
+          tc_fence_after();
+          issue_s(0, t + 1);
+        }
+        if (!mbar_wait(bar(B_PREADY + 1), t & 1, &s_abort)) break;
+        tc_fence_after();
+        issue_o(1, t);
+        tc_commit(bar(B_EMPTYV + s));
+        if (more) {
+          issue_s(1, t + 1);
+          tc_commit(bar(B_EMPTYK + s1));
+        }
+      }
     }
+    if (lane == 0) tc_commit(bar(B_ODONE));
   } else {
     // ===================== softmax group i (warps 4i .. 4i+3) =====================
     const int grp = warp >> 2;
@@ -411,17 +433,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int e_hi = edge ? (row_valid ? (int)max((int64_t)-1, min((int64_t)kKeys - 1, p_row - j0))
                                          : -1)
                             : kKeys - 1;
+      // Interior tiles (no row of the warp at a window or causal edge) skip
+      // the per-key masks entirely.
+      const bool masked = __any_sync(0xffffffffu, edge);
       // Pass 1: row maximum (S is read from TMEM twice instead of held in registers).
       float mx = -INFINITY;
 #pragma unroll
-      for (int cb = 0; cb < kKeys / 32; ++cb) {
-        uint32_t rr[32];
-        TC_LD32(tS + cb * 32, rr);
+      for (int cb = 0; cb < kKeys / 64; ++cb) {
+        uint32_t rr[64];
+        TC_LD32(tS + cb * 64, rr);        // two loads in flight before one wait
+        TC_LD32(tS + cb * 64 + 32, (rr + 32));
         tc_wait_ld();
+        if (!masked) {
+          // four independent chains keep the FMNMX latency off the critical path
+          float m2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int ee = cb * 32 + e;
-          if (ee >= e_lo && ee <= e_hi) mx = fmaxf(mx, __uint_as_float(rr[e]));
+          for (int e = 0; e < 64; ++e) m2[e & 3] = fmaxf(m2[e & 3], __uint_as_float(rr[e]));
+          mx = fmaxf(mx, fmaxf(fmaxf(m2[0], m2[1]), fmaxf(m2[2], m2[3])));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            const int ee = cb * 64 + e;
+            if (ee >= e_lo && ee <= e_hi) mx = fmaxf(mx, __uint_as_float(rr[e]));
+          }
         }
       }
       mx = mx == -INFINITY ? -INFINITY : mx * P.scale_log2;
@@ -448,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sc = P.scale_log2;
       // Pass 2: P = exp2(scale*s - m) as packed bf16 pairs, written over the S
       // columns already consumed (64-key half cb -> columns [32 cb, 32 cb + 32)).
-      float psum = 0.f;
+      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int cb = 0; cb < 2; ++cb) {
         uint32_t lo[32], hi[32];
@@ -460,18 +494,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 32; ++e) {
           const uint32_t x0 = e < 16 ? lo[2 * e] : hi[2 * e - 32];
           const uint32_t x1 = e < 16 ? lo[2 * e + 1] : hi[2 * e - 31];
-          const int k0 = cb * 64 + 2 * e;
-          float a0 = exp2f(fmaf(__uint_as_float(x0), sc, -mu));
-          float a1 = exp2f(fmaf(__uint_as_float(x1), sc, -mu));
-          if (k0 < e_lo || k0 > e_hi) a0 = 0.f;
-          if (k0 + 1 < e_lo || k0 + 1 > e_hi) a1 = 0.f;
+          float a0 = ex2(fmaf(__uint_as_float(x0), sc, -mu));
+          float a1 = ex2(fmaf(__uint_as_float(x1), sc, -mu));
+          if (masked) {
+            const int k0 = cb * 64 + 2 * e;
+            if (k0 < e_lo || k0 > e_hi) a0 = 0.f;
+            if (k0 + 1 < e_lo || k0 + 1 > e_hi) a1 = 0.f;
+          }
+          ps4[e & 3] += a0 + a1;
           __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
-          psum += __low2float(h) + __high2float(h);
           pk[e] = *reinterpret_cast<uint32_t *>(&h);
         }
         TC_ST32(tS + cb * 32, pk);
       }
-      l_run += psum;
+      l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
       tc_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_PREADY + grp));
