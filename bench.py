@@ -176,6 +176,8 @@ def run_native(args, rank, world):
                                            f"r={args.r or spec.r}, chunk={args.chunk or spec.chunk}]")
     W, K = args.warmup, args.steps
     st = DecodeState(spec, max_steps=W + 2 * K + 4)
+    if args.attn_path != -1:
+        api.swa_set_attn_path(st.ctx, args.attn_path)
     t0 = time.time()
     st.prefill()
     setup_s = time.time() - t0
@@ -437,6 +439,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="first N layers (profiling only)")
     ap.add_argument("--r", type=float, default=0.0, help="SWA/full token ratio (profiling only)")
     ap.add_argument("--chunk", type=int, default=0, help="prefill chunk (profiling only)")
+    ap.add_argument("--attn-path", type=int, default=-1,
+                    help="-1 best kernels (default); 1 cp.async decode; 0 generic (diagnostics)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -239,7 +239,6 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_decode_mma(MmaParams P) {
       cp_async16(smem_u32(st + dv), vbase + off, ok);
     }
   };
-
   __syncthreads();  // Q tile and page rows visible
 #pragma unroll
   for (int t = 0; t < kStages - 1; ++t) {
@@ -484,7 +483,7 @@ Layout layout_of(const Ctx &c, int layer, int64_t nq, int max_seq_len) {
   const int G = c.cfg.num_q_heads / L.hkv;
   w.max_splits = (max_keys_of(c, layer, max_seq_len) + kSplitKeys - 1) / kSplitKeys;
   size_t part = (size_t)nq * L.hkv * w.max_splits * G * (c.cfg.head_dim + 2) * sizeof(float);
-  w.ticket_off = (part + 255) / 256 * 256;
+  w.ticket_off = 256 + (part + 255) / 256 * 256;   // first 256 bytes: reserved counters
   w.total = w.ticket_off + ((size_t)nq * L.hkv * sizeof(int32_t) + 255) / 256 * 256;
   return w;
 }
@@ -537,7 +536,7 @@ cudaError_t launch_attn_decode_mma(Ctx &c, const AttnArgs &a, cudaStream_t s) {
   P.qk_scale_log2 = a.scale * 1.4426950408889634f * (fp8 ? a.k_scale : 1.f);
   P.v_scale = fp8 ? a.v_scale : 1.f;
   P.out = static_cast<__nv_bfloat16 *>(a.out);
-  P.partials = static_cast<float *>(a.ws);
+  P.partials = reinterpret_cast<float *>(static_cast<char *>(a.ws) + 256);
   P.tickets = reinterpret_cast<int32_t *>(static_cast<char *>(a.ws) + w.ticket_off);
   P.max_splits = w.max_splits;
   P.err = c.err_word;

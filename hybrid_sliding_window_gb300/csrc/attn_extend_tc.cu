@@ -32,7 +32,6 @@
 // Every mbarrier wait has a poll limit; on expiry the kernel sets an error
 // bit, every role leaves its loop, and the TMEM is still released.
 #include <cuda_bf16.h>
-#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -53,6 +52,7 @@ constexpr float kRescaleGap = 8.f;           // log2 units: rescale O when the m
 
 struct TcParams {
   int kind, window, hkv, G, ps, ps_shift;
+  int64_t page_stride;   // rows between consecutive pages of the layer's view
   int64_t pool_rows;
   const int32_t *rt;
   int64_t rt_stride;
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         page = 0;
       }
     }
-    s_rows[i] = page == -2 ? -1 : (int32_t)(page * P.ps);
+    s_rows[i] = page == -2 ? -1 : (int32_t)(page * P.page_stride);
   }
   for (int i = tid; i < 4 * kTileBytes / 16; i += kThreads)
     reinterpret_cast<uint4 *>(smem + kOffK)[i] = make_uint4(0, 0, 0, 0);
@@ -554,50 +554,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-bool ps_ok(int ps) { return ps >= 16 && ps <= 128 && (ps & (ps - 1)) == 0; }
-
 }  // namespace
 
-void make_kv_tensor_maps(Ctx &c, int layer) {
-  LayerInfo &L = c.layers[layer];
-  L.tma = false;
-  if (c.cfg.layout != SWA_LAYOUT_PER_LAYER || c.cfg.kv_dtype != SWA_DTYPE_BF16 ||
-      c.cfg.head_dim != kD || !ps_ok(c.cfg.page_size))
-    return;
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-  if (!fn) return;
-  const int64_t rows = (L.in_full ? c.cfg.size_full : c.cfg.size_swa) + c.cfg.page_size;
-  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)L.hkv, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)L.hkv * kD * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)c.cfg.page_size};
-  cuuint32_t estr[3] = {1, 1, 1};
-  for (int kv = 0; kv < 2; ++kv) {
-    CUresult r = fn(kv ? &L.tmv : &L.tmk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                    kv ? (void *)L.addr.v : (void *)L.addr.k, dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return;
-  }
-  L.tma = true;
-}
-
 bool tc_extend_supported(const Ctx &c, int layer) {
-  if (!c.layers[layer].tma) return false;
+  if (!c.layers[layer].tma || c.cfg.kv_dtype != SWA_DTYPE_BF16 || c.cfg.head_dim != kD ||
+      c.cfg.page_size > 64)
+    return false;
   const int G = c.cfg.num_q_heads / c.layers[layer].hkv;
   return G == 8 || G == 16;
 }
@@ -614,6 +576,7 @@ cudaError_t launch_attn_extend_tc(Ctx &c, const AttnArgs &a, cudaStream_t s) {
   P.G = c.cfg.num_q_heads / L.hkv;
   P.ps = c.cfg.page_size;
   P.ps_shift = __builtin_ctz((unsigned)P.ps);
+  P.page_stride = (int64_t)P.ps * (L.addr.blocks ? L.addr.blocks : 1);
   P.pool_rows = (L.in_full ? c.cfg.size_full : c.cfg.size_swa) + c.cfg.page_size;
   P.rt = a.rt;
   P.rt_stride = a.rt_stride;

@@ -489,15 +489,19 @@ swa_status swa_plan(swa_ctx *c, int32_t bs, const int32_t *rt, int64_t rt_stride
 }
 
 // --------------------------------------------------------------- attention ---
+static bool use_tma(const swa_ctx *c, int layer) {
+  return c->forced_path == 3 && swa::tma_decode_supported(*c, layer);
+}
 static bool use_mma(const swa_ctx *c, int layer) {
   return c->forced_path != 0 && swa::mma_decode_supported(*c, layer);
 }
 static bool use_tc(const swa_ctx *c, int layer) {
-  return c->forced_path != 0 && swa::tc_extend_supported(*c, layer);
+  return (c->forced_path == -1 || c->forced_path == 3) && swa::tc_extend_supported(*c, layer);
 }
 
 size_t swa_attn_decode_ws_bytes(const swa_ctx *c, int32_t layer, int32_t bs, int32_t max_seq_len) {
   if (!c || layer < 0 || layer >= c->cfg.num_layers || bs < 0 || max_seq_len < 1) return 0;
+  if (use_tma(c, layer)) return swa::tma_decode_ws_bytes(*c, layer, bs, max_seq_len);
   if (use_mma(c, layer)) return swa::mma_decode_ws_bytes(*c, layer, bs, max_seq_len);
   return swa::simt_ws_bytes(*c, layer, bs, max_seq_len);
 }
@@ -538,7 +542,10 @@ swa_status swa_attn_decode(swa_ctx *c, int32_t layer, int32_t bs, const int32_t 
   a.ws = ws;
   a.ws_bytes = ws_bytes;
   cudaStream_t s = (cudaStream_t)stream;
-  if (use_mma(c, layer)) {
+  if (use_tma(c, layer)) {
+    c->last_path = 3;
+    CUDA_TRY(c, swa::launch_attn_decode_tma(*c, a, s));
+  } else if (use_mma(c, layer)) {
     c->last_path = 1;
     CUDA_TRY(c, swa::launch_attn_decode_mma(*c, a, s));
   } else {
@@ -609,7 +616,7 @@ int32_t swa_last_attn_path(const swa_ctx *c) { return c ? c->last_path : -1; }
 
 swa_status swa_set_attn_path(swa_ctx *c, int32_t path) {
   if (!c) return SWA_ERR_INVALID;
-  if (path != -1 && path != 0) return fail(c, SWA_ERR_INVALID, "path must be -1 or 0");
+  if (path < -1 || path > 3 || path == 2) return fail(c, SWA_ERR_INVALID, "path must be -1, 0, 1 or 3");
   c->forced_path = path;
   return SWA_OK;
 }

@@ -156,6 +156,10 @@ bool mma_decode_supported(const Ctx &c, int layer);
 size_t mma_decode_ws_bytes(const Ctx &c, int layer, int64_t nq, int max_seq_len);
 cudaError_t launch_attn_decode_mma(Ctx &c, const AttnArgs &a, cudaStream_t s);
 
+bool tma_decode_supported(const Ctx &c, int layer);
+size_t tma_decode_ws_bytes(const Ctx &c, int layer, int64_t nq, int max_seq_len);
+cudaError_t launch_attn_decode_tma(Ctx &c, const AttnArgs &a, cudaStream_t s);
+
 bool tc_extend_supported(const Ctx &c, int layer);
 // Builds the TMA tensor maps of one layer (bf16, D = 128, per-layer layout);
 // leaves tma = false when the layer does not qualify or encoding fails.

@@ -148,8 +148,8 @@ class DecodeState:
         if spec.layout == "per_layer":
             for kind, w, hkv in spec.layers:
                 n = (nf if kind == FULL else ns) + spec.ps
-                k = torch.empty((n, hkv, spec.D), dtype=st, device=device)
-                v = torch.empty((n, hkv, spec.D), dtype=st, device=device)
+                k = torch.zeros((n, hkv, spec.D), dtype=st, device=device)
+                v = torch.zeros((n, hkv, spec.D), dtype=st, device=device)
                 if poison_page0:
                     k[:spec.ps].fill_(float("nan")) if st != torch.uint8 else k[:spec.ps].fill_(0x7F)
                     v[:spec.ps].fill_(float("nan")) if st != torch.uint8 else v[:spec.ps].fill_(0x7F)
@@ -162,9 +162,9 @@ class DecodeState:
             hs = [h for k, _, h in spec.layers if k != FULL][0]
             rb_f = hf * spec.D * ESIZE[spec.dtype]
             rb_s = hs * spec.D * ESIZE[spec.dtype]
-            self.full_env = torch.empty(((nf // spec.ps + 2) * 2 * lf * spec.ps) * rb_f,
+            self.full_env = torch.zeros(((nf // spec.ps + 2) * 2 * lf * spec.ps) * rb_f,
                                         dtype=torch.uint8, device=device)
-            self.swa_env = torch.empty(((ns // spec.ps + 2) * 2 * ls * spec.ps) * rb_s,
+            self.swa_env = torch.zeros(((ns // spec.ps + 2) * 2 * ls * spec.ps) * rb_s,
                                        dtype=torch.uint8, device=device)
             if poison_page0:
                 self.full_env[: 2 * lf * spec.ps * rb_f].fill_(0x7F)

@@ -40,6 +40,10 @@
  *   [L0_K*ps | L0_V*ps | L1_K*ps | ...]; the row of slot t of pool-layer l is
  *   kernel_id(t) + (2l or 2l+1)*ps with kernel_id(t) = (t/ps)*(ps*2L) + t%ps
  *   ([PR 34602], "implementation", step 1).
+ * - KV pools must be zero-filled when created, as the pages' pools are
+ *   ([Pools 15], "second mapping": torch.zeros): the tensor-core kernels load
+ *   whole pages, and rows of a page outside a query's key range must hold
+ *   finite values (their softmax weight is zero).
  * - Streams: swa_stream_t is a cudaStream_t (0 = legacy default stream).
  */
 #ifndef SWA_H
@@ -363,12 +367,17 @@ swa_status swa_attn_extend(swa_ctx *ctx, int32_t layer, int32_t bs,
                            swa_stream_t stream);
 
 /* Which kernel family the last attention call on ctx launched
- * (0 = generic CUDA-core kernel, 1 = tensor-core decode, 2 = tcgen05
- * extend), for tests and profiling. */
+ * (0 = generic CUDA-core kernel, 1 = tensor-core decode fed by cp.async,
+ * 2 = tcgen05 extend, 3 = persistent TMA-fed tensor-core decode), for tests
+ * and profiling. */
 int32_t swa_last_attn_path(const swa_ctx *ctx);
 /* Restricts the kernel family attention calls on ctx may take: -1 = best
- * available (default), 0 = generic CUDA-core kernel only.  Any other value
- * is SWA_ERR_INVALID.  For tests and profiling. */
+ * available (default: cp.async tensor-core decode, tcgen05 extend), 0 =
+ * generic CUDA-core kernel only, 1 = cp.async tensor-core decode and no
+ * tcgen05 extend, 3 = the persistent TMA-fed decode where it applies (an
+ * alternative decode kernel, slower than the default on the measured
+ * workloads).  Any other value is SWA_ERR_INVALID.  For tests and
+ * profiling. */
 swa_status swa_set_attn_path(swa_ctx *ctx, int32_t path);
 
 #ifdef __cplusplus
