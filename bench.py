@@ -253,13 +253,8 @@ def run_native(args, rank, world):
     e2e_max = e2e_ms
     tot_bytes = sum(bytes_steps)
     tot_e2e = e2e_bytes
-    if dist:
-        tt = torch.tensor([t_ms, e2e_ms], dtype=torch.float64, device="cuda")
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        t_ms_max, e2e_max = tt.tolist()
-        bb = torch.tensor([float(tot_bytes), float(tot_e2e)], dtype=torch.float64, device="cuda")
-        tdist.all_reduce(bb, op=tdist.ReduceOp.SUM)
-        tot_bytes, tot_e2e = bb.tolist()
+    (t_ms_max, e2e_max), (tot_bytes, tot_e2e) = reduce_ranks(
+        [t_ms, e2e_ms], [float(tot_bytes), float(tot_e2e)], "cuda")
     if rank != 0:
         return None
     peak, peak_kind = peaks()
@@ -297,12 +292,40 @@ def run_native(args, rank, world):
         "gpu_launches": st.launches_per_step() * K,
         "attn_path": api.swa_last_attn_path(st.ctx),
     }
+    if world == 1 and not args.no_extend:
+        # The other two figures the metric names: extend TFLOP/s and evict
+        # slots/s, on the chunked-prefill workload (decode pools freed first).
+        del st, inputs, host_in, dev_in, host_out
+        import gc
+        gc.collect()
+        torch.cuda.empty_cache()
+        sub = argparse.Namespace(**vars(args))
+        sub.steps, sub.warmup, sub.layers = 2, 1, 0
+        ext = run_extend(sub, rank, world)
+        line["extend"] = {k: ext[k] for k in ("value", "unit", "ms_per_step",
+                                              "frac_of_sustained_bf16", "roofline", "clocks")}
+        line["extend"]["workload"] = ext["config"]["workload"]
+        line["evict"] = ext["evict"]
     if world == 1 and not args.no_cpu:
         try:
             line["cpu_baseline"] = cpu_sample(args.workload, args.cpu_seconds)
         except Exception as e:  # the GPU number stands; say why the baseline is missing
             line["cpu_baseline"] = {"error": str(e)[:300]}
     return line
+
+
+def reduce_ranks(max_vals, sum_vals, device):
+    """Max of the times and sum of the work over ranks (any torch.distributed
+    backend); identity on a single process."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return list(max_vals), list(sum_vals)
+    mx = torch.tensor(list(max_vals), dtype=torch.float64, device=device)
+    sm = torch.tensor(list(sum_vals), dtype=torch.float64, device=device)
+    tdist.all_reduce(mx, op=tdist.ReduceOp.MAX)
+    tdist.all_reduce(sm, op=tdist.ReduceOp.SUM)
+    return mx.tolist(), sm.tolist()
 
 
 def bf16_peaks():
@@ -434,6 +457,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="mimo", choices=["mimo", "gptoss", "llama4", "extend"])
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-extend", action="store_true",
+                    help="skip the extend / evict figures added to the decode line")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--batch", type=int, default=0, help="reduced batch (profiling only)")
     ap.add_argument("--layers", type=int, default=0, help="first N layers (profiling only)")

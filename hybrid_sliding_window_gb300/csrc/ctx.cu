@@ -343,17 +343,20 @@ static swa_status alloc_common(swa_ctx *c, int32_t bs, const int64_t *pre, const
   if (!c) return SWA_ERR_INVALID;
   if (bs < 0 || bs > c->cfg.max_batch) return fail(c, SWA_ERR_INVALID, "bs out of range");
   if (bs == 0) return SWA_OK;
-  if (!seq || !seq_h || !out_full) return fail(c, SWA_ERR_INVALID, "null lengths or output");
+  if (!seq || !seq_h) return fail(c, SWA_ERR_INVALID, "null lengths");
   if (!last_loc && !rt) return fail(c, SWA_ERR_INVALID, "need last_loc or req_to_token");
   if (rt && (!req_idx || rt_stride < 1)) return fail(c, SWA_ERR_INVALID, "req_to_token needs req_idx");
   const int64_t ps = c->cfg.page_size;
-  int64_t n_new = 0;
+  int64_t n_new = 0, n_tok = 0;
   for (int b = 0; b < bs; ++b) {
     const int64_t sq = seq_h[b], pr = pre_h ? pre_h[b] : seq_h[b] - 1;
     if (pr < 0 || sq < pr) return fail(c, SWA_ERR_INVALID, "need 0 <= prefix <= seq");
     if (rt && sq > rt_stride) return fail(c, SWA_ERR_INVALID, "seq exceeds req_to_token row");
     n_new += cdiv(sq, ps) - cdiv(pr, ps);
+    n_tok += sq - pr;
   }
+  if (n_tok > 0 && !out_full) return fail(c, SWA_ERR_INVALID, "null output");
+  if (n_tok == 0) return SWA_OK;   // nothing to allocate
   cudaStream_t s = (cudaStream_t)stream;
   bool okf = ensure_pages(c, true, n_new, s);
   bool oks = ensure_pages(c, false, n_new, s);
