@@ -36,7 +36,7 @@ def _compile(src: str, verbose: bool) -> str:
     obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
     if os.path.exists(obj) and os.path.getmtime(obj) >= max(
             os.path.getmtime(src), *(os.path.getmtime(os.path.join(CSRC, h))
-                                     for h in os.listdir(CSRC) if h.endswith(".h")),
+                                     for h in os.listdir(CSRC) if h.endswith((".h", ".cuh"))),
             *(os.path.getmtime(os.path.join(INCLUDE, h)) for h in os.listdir(INCLUDE))):
         return obj
     cmd = [nvcc(), *ARCH, "-lineinfo", "-O3", "-std=c++17", "--expt-relaxed-constexpr",

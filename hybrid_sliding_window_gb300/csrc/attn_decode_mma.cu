@@ -24,6 +24,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include "split_merge.cuh"
 #include "swa_internal.h"
 
 namespace swa {
@@ -32,7 +33,6 @@ namespace {
 constexpr int kTile = 64;
 constexpr int kWarps = 4;
 constexpr int kStages = 3;
-constexpr int kSplitKeys = 1024;
 
 struct MmaParams {
   int kind, window, hkv, G, ps;
@@ -52,6 +52,7 @@ struct MmaParams {
   float *partials;
   int32_t *tickets;
   int max_splits;
+  int split_keys;         // keys per split (a multiple of the tile)
   int32_t *err;
 };
 
@@ -93,6 +94,14 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   }
+}
+
+// The SFU's base-2 exponential (denormal results flush to zero: weights below
+// 2^-126 of the row maximum).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
 }
 
 template <bool F16>
@@ -140,9 +149,14 @@ __device__ __forceinline__ int swz(int r, int c) {
   return r * (D * 2) + ((c ^ (r & 7)) << 4);
 }
 
+struct CtaSync {
+  __device__ void operator()() const { __syncthreads(); }
+};
+
 template <int D, bool FP8>
-__global__ void __launch_bounds__(kWarps * 32, 2) k_decode_mma(MmaParams P) {
+__global__ void __launch_bounds__(kWarps * 32, D == 64 ? 4 : 2) k_decode_mma(MmaParams P) {
   using S = Smem<D, FP8>;
+  static_assert(S::kTotal >= kMergeScratchBytes, "merge scratch exceeds the tiles");
   constexpr bool F16 = FP8;                 // FP8 KV widens to f16; bf16 KV stays bf16
   constexpr int kEsz = S::kEsz;
   constexpr int kRowChunks = D * kEsz / 16; // 16-byte chunks of one stored head row
@@ -161,10 +175,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_decode_mma(MmaParams P) {
   if (P.kind == SWA_LAYER_SLIDING) lo = p - P.window > 0 ? p - P.window : 0;
   else if (P.kind == SWA_LAYER_CHUNKED) lo = (p / P.window) * P.window;
   const int64_t n_keys = p - lo + 1;
-  const int n_splits = (int)((n_keys + kSplitKeys - 1) / kSplitKeys);
+  const int n_splits = (int)((n_keys + P.split_keys - 1) / P.split_keys);
   if (split >= n_splits) return;
-  const int64_t k0 = lo + (int64_t)split * kSplitKeys;
-  const int64_t k1 = min(p + 1, k0 + kSplitKeys);
+  const int64_t k0 = lo + (int64_t)split * P.split_keys;
+  const int64_t k1 = min(p + 1, k0 + P.split_keys);
   const int n_tiles = (int)((k1 - k0 + kTile - 1) / kTile);
 
   // ---- Q tile (rows >= G zero) ----
@@ -293,10 +307,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_decode_mma(MmaParams P) {
       tv = st + kTile * D * 2;
     }
     // S = Q K^T for this warp's 16 keys.
-    float s[2][4];
+    // Two accumulators per 8-key block halve the dependent mma chain.
+    float s[2][4], sx[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[nt][e] = sx[nt][e] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < D / 32; ++kk) {
         const int r = warp * 16 + nt * 8 + (lane & 7);
@@ -304,8 +320,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_decode_mma(MmaParams P) {
         uint32_t b0, b1, b2, b3;
         ldsm_x4(smem_u32(tk + swz<D>(r, c)), b0, b1, b2, b3);
         mma16816<F16>(s[nt], qa[2 * kk], b0, b1);
-        mma16816<F16>(s[nt], qa[2 * kk + 1], b2, b3);
+        mma16816<F16>(sx[nt], qa[2 * kk + 1], b2, b3);
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[nt][e] += sx[nt][e];
     }
     // Scale, mask, online softmax (rows g and g+8).
     const int64_t kbase_j = k0 + (int64_t)t * kTile + warp * 16;
@@ -329,27 +347,29 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_decode_mma(MmaParams P) {
     const float mn0 = fmaxf(m0, rmax0), mn1 = fmaxf(m1, rmax1);
     const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
     const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float corr0 = exp2f(m0 - mu0), corr1 = exp2f(m1 - mu1);
+    const float corr0 = ex2(m0 - mu0), corr1 = ex2(m1 - mu1);
     m0 = mn0;
     m1 = mn1;
     float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      s[nt][0] = exp2f(s[nt][0] - mu0);
-      s[nt][1] = exp2f(s[nt][1] - mu0);
-      s[nt][2] = exp2f(s[nt][2] - mu1);
-      s[nt][3] = exp2f(s[nt][3] - mu1);
+      s[nt][0] = ex2(s[nt][0] - mu0);
+      s[nt][1] = ex2(s[nt][1] - mu0);
+      s[nt][2] = ex2(s[nt][2] - mu1);
+      s[nt][3] = ex2(s[nt][3] - mu1);
       ps0 += s[nt][0] + s[nt][1];
       ps1 += s[nt][2] + s[nt][3];
     }
     l0 = l0 * corr0 + ps0;
     l1 = l1 * corr1 + ps1;
+    if (__any_sync(0xffffffffu, corr0 != 1.f || corr1 != 1.f)) {   // a row maximum moved
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-      o[n][0] *= corr0;
-      o[n][1] *= corr0;
-      o[n][2] *= corr1;
-      o[n][3] *= corr1;
+      for (int n = 0; n < D / 8; ++n) {
+        o[n][0] *= corr0;
+        o[n][1] *= corr0;
+        o[n][2] *= corr1;
+        o[n][3] *= corr1;
+      }
     }
     uint32_t pa[4];
     pa[0] = pack2<F16>(s[0][0], s[0][1]);
@@ -396,9 +416,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_decode_mma(MmaParams P) {
   __syncthreads();
 
   const bool single = n_splits == 1;
-  const int stride = G * (D + 2);
-  const int64_t item = ((int64_t)b * P.hkv + kvh) * P.max_splits + split;
-  float *part = P.partials + item * stride;
+  const int pstride = part_stride(G, D);
+  const int64_t pair = (int64_t)b * P.hkv + kvh;
+  float *part = P.partials + (pair * P.max_splits + split) * pstride;
   for (int e = tid; e < G * D; e += blockDim.x) {
     const int gg = e / D, d = e % D;
     float M = -INFINITY;
@@ -423,10 +443,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_decode_mma(MmaParams P) {
       P.out[((int64_t)b * Hq + kvh * G + gg) * D + d] =
           __float2bfloat16_rn(A * r * P.v_scale / (L * r + extra));
     } else {
-      part[gg * (D + 2) + 2 + d] = A;
+      part[gg * D + d] = A;
       if (d == 0) {
-        part[gg * (D + 2)] = Mu;
-        part[gg * (D + 2) + 1] = L;
+        part[G * D + 2 * gg] = Mu;
+        part[G * D + 2 * gg + 1] = L;
       }
     }
   }
@@ -435,33 +455,16 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_decode_mma(MmaParams P) {
   __threadfence();
   __syncthreads();
   if (tid == 0) {
-    const int prev = atomicAdd(&P.tickets[(int64_t)b * P.hkv + kvh], 1);
+    const int prev = atomicAdd(&P.tickets[pair], 1);
     s_last = prev == n_splits - 1;
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  const float *base = P.partials + ((int64_t)b * P.hkv + kvh) * P.max_splits * stride;
-  for (int e = tid; e < G * D; e += blockDim.x) {
-    const int gg = e / D, d = e % D;
-    float M = -INFINITY;
-    for (int s = 0; s < n_splits; ++s) M = fmaxf(M, __ldcg(base + s * stride + gg * (D + 2)));
-    float Mf = M, extra = 0.f;
-    if (P.sinks) {
-      const float sg = P.sinks[kvh * G + gg] * 1.4426950408889634f;
-      Mf = fmaxf(M, sg);
-      extra = exp2f(sg - Mf);
-    }
-    float L = extra, A = 0.f;
-    for (int s = 0; s < n_splits; ++s) {
-      const float *q = base + s * stride + gg * (D + 2);
-      const float f = exp2f(__ldcg(q) - Mf);
-      L += __ldcg(q + 1) * f;
-      A += __ldcg(q + 2 + d) * f;
-    }
-    P.out[((int64_t)b * Hq + kvh * G + gg) * D + d] = __float2bfloat16_rn(A * P.v_scale / L);
-  }
-  if (tid == 0) P.tickets[(int64_t)b * P.hkv + kvh] = 0;
+  merge_split_partials<D, kWarps * 32, 4>(P.partials + pair * P.max_splits * pstride, n_splits, G,
+                                      P.sinks ? P.sinks + kvh * G : nullptr, P.v_scale,
+                                      P.out + ((int64_t)b * Hq + kvh * G) * D, P.tickets + pair,
+                                      reinterpret_cast<float *>(smem), tid, CtaSync());
 }
 
 int max_keys_of(const Ctx &c, int layer, int max_seq_len) {
@@ -474,15 +477,18 @@ int max_keys_of(const Ctx &c, int layer, int max_seq_len) {
 
 struct Layout {
   size_t ticket_off, total;
-  int max_splits;
+  int max_splits, split_keys;
 };
 
 Layout layout_of(const Ctx &c, int layer, int64_t nq, int max_seq_len) {
   Layout w;
   const LayerInfo &L = c.layers[layer];
   const int G = c.cfg.num_q_heads / L.hkv;
-  w.max_splits = (max_keys_of(c, layer, max_seq_len) + kSplitKeys - 1) / kSplitKeys;
-  size_t part = (size_t)nq * L.hkv * w.max_splits * G * (c.cfg.head_dim + 2) * sizeof(float);
+  const int mk = max_keys_of(c, layer, max_seq_len);
+  w.split_keys = decode_split_keys(c.num_sms, nq, L.hkv, mk, c.cfg.page_size,
+                                   c.cfg.head_dim * (c.cfg.kv_dtype == SWA_DTYPE_E4M3 ? 1 : 2));
+  w.max_splits = (mk + w.split_keys - 1) / w.split_keys;
+  size_t part = (size_t)nq * L.hkv * w.max_splits * part_stride(G, c.cfg.head_dim) * sizeof(float);
   w.ticket_off = 256 + (part + 255) / 256 * 256;   // first 256 bytes: reserved counters
   w.total = w.ticket_off + ((size_t)nq * L.hkv * sizeof(int32_t) + 255) / 256 * 256;
   return w;
@@ -491,7 +497,7 @@ Layout layout_of(const Ctx &c, int layer, int64_t nq, int max_seq_len) {
 template <int D, bool FP8>
 cudaError_t launch_t(dim3 grid, const MmaParams &P, cudaStream_t s) {
   // Main tiles (or merge scratch), then the split's page-row table.
-  const int smem = Smem<D, FP8>::kTotal + (kSplitKeys / P.ps + 2) * (int)sizeof(int64_t);
+  const int smem = Smem<D, FP8>::kTotal + (P.split_keys / P.ps + 2) * (int)sizeof(int64_t);
   cudaError_t e = cudaFuncSetAttribute(k_decode_mma<D, FP8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -539,6 +545,7 @@ cudaError_t launch_attn_decode_mma(Ctx &c, const AttnArgs &a, cudaStream_t s) {
   P.partials = reinterpret_cast<float *>(static_cast<char *>(a.ws) + 256);
   P.tickets = reinterpret_cast<int32_t *>(static_cast<char *>(a.ws) + w.ticket_off);
   P.max_splits = w.max_splits;
+  P.split_keys = w.split_keys;
   P.err = c.err_word;
   dim3 grid(L.hkv, w.max_splits, a.nq);
   const int D = c.cfg.head_dim;

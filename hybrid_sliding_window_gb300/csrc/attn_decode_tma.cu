@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include "split_merge.cuh"
 #include "swa_internal.h"
 
 namespace swa {
@@ -41,8 +42,8 @@ namespace {
 constexpr int kTileKeys = 64;
 constexpr int kConsumers = 4;
 constexpr int kThreads = (kConsumers + 1) * 32;
-constexpr int kSplitKeys = 1024;
-constexpr int kMaxPg = kSplitKeys / 16 + 2;   // page rows of one item (ps >= 16)
+constexpr int kMaxSplitKeys = 8192;
+constexpr int kMaxPg = kMaxSplitKeys / 16 + 2;   // page rows of one item (ps >= 16)
 constexpr long kSpinLimit = 1L << 24;
 
 struct Params {
@@ -64,6 +65,7 @@ struct Params {
   int32_t *tickets;
   int32_t *work;         // [0] next item, [1] CTAs finished (reset by the last CTA)
   int max_splits;
+  int split_keys;         // keys per work item (a multiple of the tile)
   int32_t *err;
 };
 
@@ -88,6 +90,7 @@ struct Cfg {
   static constexpr int kOffRows = kOffMerge + kMergeO + kMergeML;
   static constexpr int kOffBars = kOffRows + kMaxPg * 4;
   static constexpr int kBytes = kOffBars + 2 * kStages * 8 + 64;
+  static_assert(kMergeO >= kMergeScratchBytes, "split merge scratch exceeds the merge buffers");
 };
 
 // ------------------------------------------------------------------ PTX ---
@@ -133,6 +136,9 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
 }
+struct ConsumerSync {   // barrier 1 over the consumer warps
+  __device__ void operator()() const { named_sync(1, kConsumers * 32); }
+};
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                         uint32_t &r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -207,11 +213,11 @@ __device__ __forceinline__ bool find_item(const Params &P, const int *s_pref, in
   const int local = idx - s_pref[lo];
   const int64_t p = P.seq[lo] - 1;
   it.lo = key_lo(P.kind, P.window, p);
-  it.n_splits = (int)((p - it.lo + 1 + kSplitKeys - 1) / kSplitKeys);
+  it.n_splits = (int)((p - it.lo + 1 + P.split_keys - 1) / P.split_keys);
   it.kvh = local % P.hkv;                 // heads of one split adjacent: rows shared in DRAM
   it.split = local / P.hkv;
-  it.k0 = it.lo + (int64_t)it.split * kSplitKeys;
-  it.k1 = min(p + 1, it.k0 + kSplitKeys);
+  it.k0 = it.lo + (int64_t)it.split * P.split_keys;
+  it.k1 = min(p + 1, it.k0 + P.split_keys);
   return true;
 }
 
@@ -241,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       s_pref[b] = acc;
       const int64_t p = P.seq[b] - 1;
       const int64_t lo = key_lo(P.kind, P.window, p);
-      acc += (int)((p - lo + 1 + kSplitKeys - 1) / kSplitKeys) * P.hkv;
+      acc += (int)((p - lo + 1 + P.split_keys - 1) / P.split_keys) * P.hkv;
     }
     s_pref[P.bs] = acc;
     s_abort = 0;
@@ -289,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int n_tiles = (int)((it.k1 - 1 - kt0) / kTileKeys + 1);
       const int64_t pg0 = kt0 / P.ps;
       const int n_pg = (int)((it.k1 - 1) / P.ps - pg0 + 1);
-      if (n_pg > kMaxPg || n_tiles > kSplitKeys / kTileKeys + 1) {   // cannot happen for ps >= 16
+      if (n_pg > kMaxPg || n_tiles > P.split_keys / kTileKeys + 1) {   // cannot happen for ps >= 16
         if (lane == 0) {
           set_error(P.err, SWA_DEVERR_RANGE);
           s_abort = 1;
@@ -553,9 +559,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       named_sync(1, kConsumers * 32);
       const bool single = it.n_splits == 1;
-      const int stride = G * (D + 2);
+      const int pstride = part_stride(G, D);
       const int64_t bh = (int64_t)it.b * P.hkv + it.kvh;
-      float *part = P.partials + (bh * P.max_splits + it.split) * stride;
+      float *part = P.partials + (bh * P.max_splits + it.split) * pstride;
       for (int e = tid; e < G * D; e += kConsumers * 32) {
         const int gg = e / D, d = e % D;
         float M = -INFINITY;
@@ -580,10 +586,10 @@ __global__ void __launch_bounds__(kThreads, 2)
           P.out[((int64_t)it.b * Hq + it.kvh * G + gg) * D + d] =
               __float2bfloat16_rn(A * r * P.v_scale / (L * r + extra));
         } else {
-          part[gg * (D + 2) + 2 + d] = A;
+          part[gg * D + d] = A;
           if (d == 0) {
-            part[gg * (D + 2)] = Mu;
-            part[gg * (D + 2) + 1] = L;
+            part[G * D + 2 * gg] = Mu;
+            part[G * D + 2 * gg + 1] = L;
           }
         }
       }
@@ -594,29 +600,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         named_sync(1, kConsumers * 32);
         if (s_last) {
           __threadfence();
-          const float *base = P.partials + bh * P.max_splits * stride;
-          for (int e = tid; e < G * D; e += kConsumers * 32) {
-            const int gg = e / D, d = e % D;
-            float M = -INFINITY;
-            for (int s2 = 0; s2 < it.n_splits; ++s2)
-              M = fmaxf(M, __ldcg(base + s2 * stride + gg * (D + 2)));
-            float Mf = M, extra = 0.f;
-            if (P.sinks) {
-              const float sg = P.sinks[it.kvh * G + gg] * 1.4426950408889634f;
-              Mf = fmaxf(M, sg);
-              extra = ex2(sg - Mf);
-            }
-            float L = extra, A = 0.f;
-            for (int s2 = 0; s2 < it.n_splits; ++s2) {
-              const float *qp = base + s2 * stride + gg * (D + 2);
-              const float f = ex2(__ldcg(qp) - Mf);
-              L += __ldcg(qp + 1) * f;
-              A += __ldcg(qp + 2 + d) * f;
-            }
-            P.out[((int64_t)it.b * Hq + it.kvh * G + gg) * D + d] =
-                __float2bfloat16_rn(A * P.v_scale / L);
-          }
-          if (tid == 0) P.tickets[bh] = 0;
+          merge_split_partials<D, kConsumers * 32, 1>(
+              P.partials + bh * P.max_splits * pstride, it.n_splits, G,
+              P.sinks ? P.sinks + it.kvh * G : nullptr, P.v_scale,
+              P.out + ((int64_t)it.b * Hq + it.kvh * G) * D, P.tickets + bh, sm_o, tid,
+              ConsumerSync());
         }
       }
       named_sync(1, kConsumers * 32);   // merge buffers and Q tile free for the next item
@@ -667,13 +655,31 @@ bool tma_decode_supported(const Ctx &c, int layer) {
   return c.cfg.kv_dtype == SWA_DTYPE_E4M3 && D == 128;
 }
 
-size_t tma_decode_ws_bytes(const Ctx &c, int layer, int64_t nq, int max_seq_len) {
+// Workspace: [work counters, 256 B][partials][tickets]; every decode kernel
+// family keeps its partials past the first 256 bytes, so the counters survive
+// layers of different shapes sharing one workspace.
+struct WsLayout {
+  int split_keys, max_splits;
+  size_t ticket_off, total;
+};
+
+static WsLayout ws_layout(const Ctx &c, int layer, int64_t nq, int max_seq_len) {
   const LayerInfo &L = c.layers[layer];
   const int G = c.cfg.num_q_heads / L.hkv;
-  const int max_splits = (max_keys_of(c, layer, max_seq_len) + kSplitKeys - 1) / kSplitKeys;
-  const size_t part = (size_t)nq * L.hkv * max_splits * G * (c.cfg.head_dim + 2) * sizeof(float);
-  const size_t toff = 256 + (part + 255) / 256 * 256;
-  return toff + ((size_t)nq * L.hkv * sizeof(int32_t) + 255) / 256 * 256;
+  const int mk = max_keys_of(c, layer, max_seq_len);
+  WsLayout w;
+  w.split_keys = decode_split_keys(c.num_sms, nq, L.hkv, mk, c.cfg.page_size,
+                                   c.cfg.head_dim * (c.cfg.kv_dtype == SWA_DTYPE_E4M3 ? 1 : 2));
+  if (w.split_keys > kMaxSplitKeys) w.split_keys = kMaxSplitKeys;
+  w.max_splits = (mk + w.split_keys - 1) / w.split_keys;
+  const size_t part = (size_t)nq * L.hkv * w.max_splits * part_stride(G, c.cfg.head_dim) * sizeof(float);
+  w.ticket_off = 256 + (part + 255) / 256 * 256;
+  w.total = w.ticket_off + ((size_t)nq * L.hkv * sizeof(int32_t) + 255) / 256 * 256;
+  return w;
+}
+
+size_t tma_decode_ws_bytes(const Ctx &c, int layer, int64_t nq, int max_seq_len) {
+  return ws_layout(c, layer, nq, max_seq_len).total;
 }
 
 cudaError_t launch_attn_decode_tma(Ctx &c, const AttnArgs &a, cudaStream_t s) {
@@ -700,14 +706,12 @@ cudaError_t launch_attn_decode_tma(Ctx &c, const AttnArgs &a, cudaStream_t s) {
   P.qk_scale_log2 = a.scale * 1.4426950408889634f * (fp8 ? a.k_scale : 1.f);
   P.v_scale = fp8 ? a.v_scale : 1.f;
   P.out = static_cast<__nv_bfloat16 *>(a.out);
-  P.max_splits = (max_keys_of(c, a.layer, a.max_seq_len) + kSplitKeys - 1) / kSplitKeys;
-  const size_t part = (size_t)a.nq * L.hkv * P.max_splits * G * (c.cfg.head_dim + 2) * sizeof(float);
-  // Workspace: [work counters, 256 B][partials][tickets]; every decode kernel
-  // family keeps its partials past the first 256 bytes, so the counters
-  // survive layers of different shapes sharing one workspace.
+  const WsLayout w = ws_layout(c, a.layer, a.nq, a.max_seq_len);
+  P.split_keys = w.split_keys;
+  P.max_splits = w.max_splits;
   P.work = static_cast<int32_t *>(a.ws);
   P.partials = reinterpret_cast<float *>(static_cast<char *>(a.ws) + 256);
-  P.tickets = reinterpret_cast<int32_t *>(static_cast<char *>(a.ws) + 256 + (part + 255) / 256 * 256);
+  P.tickets = reinterpret_cast<int32_t *>(static_cast<char *>(a.ws) + w.ticket_off);
   P.err = c.err_word;
   if (fp8) return launch_t<128, true>(c, L, P, s);
   if (c.cfg.head_dim == 128) return launch_t<128, false>(c, L, P, s);
