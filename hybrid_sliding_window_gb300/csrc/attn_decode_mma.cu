@@ -14,7 +14,8 @@
 // 3-stage cp.async pipeline (16-byte gathers of whole K/V rows, row address
 // from the index tables, out-of-range rows zero-filled without a read), each
 // warp owning 16 keys of every tile with its own online-softmax state in
-// registers.  FP8 tiles are widened to f16 in shared memory (E4M3 is a subset
+// registers.  FP8 rows are converted to f16 in registers on their way to
+// the tensor cores (E4M3 is a subset
 // of f16; the scales fold into the score scale and the output).  Splits of
 // one (request, KV head) meet through an atomic ticket: the last CTA merges
 // the partials and the sink, so one launch does split and merge.
@@ -32,7 +33,6 @@ namespace {
 
 constexpr int kTile = 64;
 constexpr int kWarps = 4;
-constexpr int kStages = 3;
 
 struct MmaParams {
   int kind, window, hkv, G, ps;
@@ -131,16 +131,19 @@ __device__ __forceinline__ int64_t key_slot(const MmaParams &P, int b, int64_t j
 // Shared-memory plan (bytes):
 //   Q tile      16 x D  16-bit, swizzled                      : 32*D
 //   stages      kStages x (K,V) 64 x D stored elements         : kStages*2*64*D*esz
-//   FP8 only:   widened K,V tile 64 x D f16, swizzled          : 2*64*D*2
-template <int D, bool FP8>
+// Heads-as-rows (G > 8) FP8 stages are half the size of bf16 ones, so twice
+// as many fit at 2 CTAs per SM; keys-as-rows kernels need fewer registers and
+// run 4 CTAs per SM where the tiles allow.
+template <int D, bool FP8, bool KM>
 struct Smem {
   static constexpr int kEsz = FP8 ? 1 : 2;
+  static constexpr int kStages = (FP8 && !KM) ? 6 : 3;
   static constexpr int kQ = 16 * D * 2;
   static constexpr int kStageBytes = 2 * kTile * D * kEsz;
-  static constexpr int kWide = FP8 ? 2 * kTile * D * 2 : 0;
   static constexpr int kMerge = kWarps * 16 * (D + 4) * 4 + 2 * kWarps * 16 * 4;
-  static constexpr int kMain = kQ + kStages * kStageBytes + kWide;
+  static constexpr int kMain = kQ + kStages * kStageBytes;
   static constexpr int kTotal = kMain > kMerge ? kMain : kMerge;
+  static constexpr int kMinBlocks = (D == 64 || (KM && FP8)) ? 4 : 2;
 };
 
 // 16-bit tile addressing: row r, 16-byte chunk c (D/8 chunks per row), XOR swizzle.
@@ -149,27 +152,76 @@ __device__ __forceinline__ int swz(int r, int c) {
   return r * (D * 2) + ((c ^ (r & 7)) << 4);
 }
 
+// FP8 tiles: row r of D bytes, 16-byte chunk c.  K rows are read by ldmatrix
+// (eight rows, one chunk), V rows as 32-bit words by lanes that own key pairs
+// (2c4, 2c4+1): each tile has the swizzle that keeps its reads free of bank
+// conflicts (for D = 128; D = 64 V reads are two-way).
+template <int D>
+__device__ __forceinline__ int kswz8(int r, int c) {
+  return r * D + ((c ^ (D == 128 ? (r & 7) : ((r >> 1) & 3))) << 4);
+}
+template <int D>
+__device__ __forceinline__ int vswz8(int r, int c) {
+  return r * D + ((c ^ (D == 128 ? 2 * ((r >> 1) & 3) : 2 * ((r >> 1) & 1))) << 4);
+}
+
+// Two E4M3 values (low byte first) to an f16 pair; exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v & 0xffffu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// Transpose of an 8x8 16-bit block held one row-pair per lane.
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+
 struct CtaSync {
   __device__ void operator()() const { __syncthreads(); }
 };
 
-template <int D, bool FP8>
-__global__ void __launch_bounds__(kWarps * 32, D == 64 ? 4 : 2) k_decode_mma(MmaParams P) {
-  using S = Smem<D, FP8>;
+// Two orientations of the per-warp products (16 keys of each 64-key tile per
+// warp):
+//  * heads as rows (KM = false, G <= 16): S = Q K^T with the G heads as the
+//    M = 16 rows, then O += P V;
+//  * keys as rows (KM = true, G <= 8): S^T = K Q^T with the 16 keys as M and
+//    the heads as N = 8, then O^T += V^T P^T, P^T transposed in registers.
+//    Half the tensor-core work when the group has at most 8 heads, and half
+//    the accumulator registers.
+template <int D, bool FP8, bool KM>
+__global__ void __launch_bounds__(kWarps * 32, (Smem<D, FP8, KM>::kMinBlocks))
+    k_decode_mma(MmaParams P) {
+  using S = Smem<D, FP8, KM>;
   static_assert(S::kTotal >= kMergeScratchBytes, "merge scratch exceeds the tiles");
   constexpr bool F16 = FP8;                 // FP8 KV widens to f16; bf16 KV stays bf16
+  constexpr int kStages = S::kStages;
   constexpr int kEsz = S::kEsz;
   constexpr int kRowChunks = D * kEsz / 16; // 16-byte chunks of one stored head row
   extern __shared__ __align__(128) char smem[];
   char *sq = smem;
   char *sstage = smem + S::kQ;
-  char *swide = sstage + kStages * S::kStageBytes;
 
   // KV heads fastest: the CTAs of all heads of the same keys run together, so
   // each token's interleaved head rows are read from DRAM at about one time.
   const int kvh = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = P.G;
+  const int Hq = P.hkv * G;
+
+  // ---- Q rows into registers first: their latency hides behind the
+  // page-row lookups and the first tile loads ----
+  constexpr int kQPer = 16 * (D / 8) / (kWarps * 32);
+  uint4 qv[kQPer];
+#pragma unroll
+  for (int k = 0; k < kQPer; ++k) {
+    const int i = tid + k * kWarps * 32;
+    const int r = i / (D / 8), c = i % (D / 8);
+    qv[k] = make_uint4(0, 0, 0, 0);
+    if (r < G) qv[k] = *reinterpret_cast<const uint4 *>(P.q + ((int64_t)b * Hq + kvh * G + r) * D + c * 8);
+  }
+
   const int64_t p = P.seq[b] - 1;
   int64_t lo = 0;
   if (P.kind == SWA_LAYER_SLIDING) lo = p - P.window > 0 ? p - P.window : 0;
@@ -180,24 +232,6 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 4 : 2) k_decode_mma(Mma
   const int64_t k0 = lo + (int64_t)split * P.split_keys;
   const int64_t k1 = min(p + 1, k0 + P.split_keys);
   const int n_tiles = (int)((k1 - k0 + kTile - 1) / kTile);
-
-  // ---- Q tile (rows >= G zero) ----
-  const int Hq = P.hkv * G;
-  for (int i = tid; i < 16 * (D / 8); i += blockDim.x) {
-    const int r = i / (D / 8), c = i % (D / 8);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < G) {
-      v = *reinterpret_cast<const uint4 *>(P.q + ((int64_t)b * Hq + kvh * G + r) * D + c * 8);
-      if constexpr (F16) {
-        __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(&v);
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) w[e] = pack2<true>(__bfloat162float(h[2 * e]), __bfloat162float(h[2 * e + 1]));
-        v = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    }
-    *reinterpret_cast<uint4 *>(sq + swz<D>(r, c)) = v;
-  }
 
   // ---- page rows of this split, looked up once (one table read per page) ----
   // Positions of one page occupy consecutive slots of one pool page, so the
@@ -243,8 +277,8 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 4 : 2) k_decode_mma(Mma
       }
       int dk, dv;
       if constexpr (FP8) {
-        dk = r * D + c * 16;                         // raw bytes, not swizzled
-        dv = kTile * D + r * D + c * 16;
+        dk = kswz8<D>(r, c);
+        dv = kTile * D + vswz8<D>(r, c);
       } else {
         dk = swz<D>(r, c);
         dv = kTile * D * 2 + swz<D>(r, c);
@@ -253,26 +287,69 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 4 : 2) k_decode_mma(Mma
       cp_async16(smem_u32(st + dv), vbase + off, ok);
     }
   };
-  __syncthreads();  // Q tile and page rows visible
+  __syncthreads();  // page rows visible
 #pragma unroll
   for (int t = 0; t < kStages - 1; ++t) {
     if (t < n_tiles) load_tile(t);
     cp_commit();
   }
 
-  uint32_t qa[D / 16][4];
+  // ---- Q tile (rows >= G zero), f16 for FP8 KV ----
+#pragma unroll
+  for (int k = 0; k < kQPer; ++k) {
+    const int i = tid + k * kWarps * 32;
+    const int r = i / (D / 8), c = i % (D / 8);
+    uint4 v = qv[k];
+    if constexpr (F16) {
+      const __nv_bfloat16 *h = reinterpret_cast<const __nv_bfloat16 *>(&v);
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) w[e] = pack2<true>(__bfloat162float(h[2 * e]), __bfloat162float(h[2 * e + 1]));
+      v = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    *reinterpret_cast<uint4 *>(sq + swz<D>(r, c)) = v;
+  }
+  __syncthreads();  // Q tile visible
+
+  const int g = lane >> 2, c4 = lane & 3;
+  // Q fragments.  FP8: the K fragments of a 16-dim step carry dims 4c4, 4c4+1
+  // at k = 2c4, 2c4+1 and dims 4c4+2, 4c4+3 at k = 2c4+8, 2c4+9 (one 32-bit
+  // word of E4M3 per key row), so Q takes the same order of dims.
+  constexpr int kQF = KM ? 2 : 4;
+  uint32_t qa[D / 16][kQF];
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
-    const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
-    const int c = ks * 2 + (lane >> 4);
-    ldsm_x4(smem_u32(sq + swz<D>(r, c)), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+    if constexpr (KM) {   // B = Q^T: head g, two dim pairs
+      const char *r0 = FP8 ? sq + swz<D>(g, 2 * ks + (c4 >> 1)) + (c4 & 1) * 8
+                           : sq + swz<D>(g, 2 * ks) + 4 * c4;
+      qa[ks][0] = *reinterpret_cast<const uint32_t *>(r0);
+      qa[ks][1] = FP8 ? *reinterpret_cast<const uint32_t *>(r0 + 4)
+                      : *reinterpret_cast<const uint32_t *>(sq + swz<D>(g, 2 * ks + 1) + 4 * c4);
+    } else if constexpr (FP8) {
+      const int off = (c4 & 1) * 8;
+      const char *r0 = sq + swz<D>(g, 2 * ks + (c4 >> 1)) + off;
+      const char *r1 = sq + swz<D>(g + 8, 2 * ks + (c4 >> 1)) + off;
+      qa[ks][0] = *reinterpret_cast<const uint32_t *>(r0);
+      qa[ks][1] = *reinterpret_cast<const uint32_t *>(r1);
+      qa[ks][2] = *reinterpret_cast<const uint32_t *>(r0 + 4);
+      qa[ks][3] = *reinterpret_cast<const uint32_t *>(r1 + 4);
+    } else {
+      const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int c = ks * 2 + (lane >> 4);
+      uint32_t *f = qa[ks];
+      ldsm_x4(smem_u32(sq + swz<D>(r, c)), f[0], f[1], f[2], f[3]);
+    }
   }
 
-  float o[D / 8][4];
+  // Accumulators.  Heads as rows: o[n] = O[heads g, g+8][dims of block n];
+  // m0/l0 row g, m1/l1 row g+8.  Keys as rows: o[mt] = O^T[dims of block mt]
+  // [heads 2c4, 2c4+1]; m0/l0 head 2c4, m1/l1 head 2c4+1 (l per lane until
+  // the end).
+  constexpr int kOB = KM ? D / 16 : D / 8;
+  float o[kOB][4];
 #pragma unroll
-  for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  for (int n = 0; n < kOB; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  const int g = lane >> 2, c4 = lane & 3;
 
   for (int t = 0; t < n_tiles; ++t) {
     cp_wait<kStages - 2>();
@@ -280,138 +357,278 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 4 : 2) k_decode_mma(Mma
     if (t + kStages - 1 < n_tiles) load_tile(t + kStages - 1);
     cp_commit();
     const char *st = sstage + (t % kStages) * S::kStageBytes;
-    const char *tk;
-    const char *tv;
-    if constexpr (FP8) {
-      // Widen this tile to f16 (swizzled), 8 elements per thread-step.
-      for (int i = tid; i < 2 * kTile * (D / 8); i += blockDim.x) {
-        const int half = i / (kTile * (D / 8));
-        const int rem = i % (kTile * (D / 8));
-        const int r = rem / (D / 8), c = rem % (D / 8);
-        const uint2 raw = *reinterpret_cast<const uint2 *>(st + half * kTile * D + r * D + c * 8);
-        const __nv_fp8x2_storage_t *f = reinterpret_cast<const __nv_fp8x2_storage_t *>(&raw);
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(f[e], __NV_E4M3);
-          w[e] = (uint32_t)hr.x | ((uint32_t)hr.y << 16);
-        }
-        *reinterpret_cast<uint4 *>(swide + half * kTile * D * 2 + swz<D>(r, c)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      __syncthreads();
-      tk = swide;
-      tv = swide + kTile * D * 2;
-    } else {
-      tk = st;
-      tv = st + kTile * D * 2;
-    }
-    // S = Q K^T for this warp's 16 keys.
-    // Two accumulators per 8-key block halve the dependent mma chain.
-    float s[2][4], sx[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s[nt][e] = sx[nt][e] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < D / 32; ++kk) {
-        const int r = warp * 16 + nt * 8 + (lane & 7);
-        const int c = kk * 4 + (lane >> 3);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(smem_u32(tk + swz<D>(r, c)), b0, b1, b2, b3);
-        mma16816<F16>(s[nt], qa[2 * kk], b0, b1);
-        mma16816<F16>(sx[nt], qa[2 * kk + 1], b2, b3);
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s[nt][e] += sx[nt][e];
-    }
-    // Scale, mask, online softmax (rows g and g+8).
+    const char *tv = st + kTile * D * kEsz;
     const int64_t kbase_j = k0 + (int64_t)t * kTile + warp * 16;
-    float rmax0 = -INFINITY, rmax1 = -INFINITY;
+    if constexpr (KM) {
+      // ---- S^T = K Q^T: rows = this warp's 16 keys, columns = heads ----
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      const int kr = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+      if constexpr (FP8) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+        for (int kp = 0; kp < D / 32; ++kp) {   // two 16-dim steps per ldmatrix
+          uint32_t w[4];
+          ldsm_x4(smem_u32(st + kswz8<D>(kr, 2 * kp + (lane >> 4))), w[0], w[1], w[2], w[3]);
+          const uint32_t a0[4] = {e4m3x2_to_f16x2(w[0]), e4m3x2_to_f16x2(w[1]),
+                                  e4m3x2_to_f16x2(w[0] >> 16), e4m3x2_to_f16x2(w[1] >> 16)};
+          const uint32_t a1[4] = {e4m3x2_to_f16x2(w[2]), e4m3x2_to_f16x2(w[3]),
+                                  e4m3x2_to_f16x2(w[2] >> 16), e4m3x2_to_f16x2(w[3] >> 16)};
+          mma16816<true>(sa, a0, qa[2 * kp][0], qa[2 * kp][1]);
+          mma16816<true>(sb, a1, qa[2 * kp + 1][0], qa[2 * kp + 1][1]);
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          uint32_t a[4];
+          ldsm_x4(smem_u32(st + swz<D>(kr, 2 * ks + (lane >> 4))), a[0], a[1], a[2], a[3]);
+          mma16816<false>((ks & 1) ? sb : sa, a, qa[ks][0], qa[ks][1]);
+        }
+      }
+      // sa: (key g, head 2c4), (key g, head 2c4+1), (key g+8, head 2c4), (key g+8, head 2c4+1)
+      float v[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int64_t j = kbase_j + nt * 8 + 2 * c4 + (e & 1);
-        float v = s[nt][e] * P.qk_scale_log2;
-        if (j >= k1) v = -INFINITY;
-        s[nt][e] = v;
+        v[e] = (sa[e] + sb[e]) * P.qk_scale_log2;
+        if (kbase_j + g + (e >> 1) * 8 >= k1) v[e] = -INFINITY;
       }
-      rmax0 = fmaxf(rmax0, fmaxf(s[nt][0], s[nt][1]));
-      rmax1 = fmaxf(rmax1, fmaxf(s[nt][2], s[nt][3]));
-    }
-    rmax0 = fmaxf(rmax0, __shfl_xor_sync(0xffffffffu, rmax0, 1));
-    rmax0 = fmaxf(rmax0, __shfl_xor_sync(0xffffffffu, rmax0, 2));
-    rmax1 = fmaxf(rmax1, __shfl_xor_sync(0xffffffffu, rmax1, 1));
-    rmax1 = fmaxf(rmax1, __shfl_xor_sync(0xffffffffu, rmax1, 2));
-    const float mn0 = fmaxf(m0, rmax0), mn1 = fmaxf(m1, rmax1);
-    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float corr0 = ex2(m0 - mu0), corr1 = ex2(m1 - mu1);
-    m0 = mn0;
-    m1 = mn1;
-    float ps0 = 0.f, ps1 = 0.f;
+      float r0 = fmaxf(v[0], v[2]), r1 = fmaxf(v[1], v[3]);
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      s[nt][0] = ex2(s[nt][0] - mu0);
-      s[nt][1] = ex2(s[nt][1] - mu0);
-      s[nt][2] = ex2(s[nt][2] - mu1);
-      s[nt][3] = ex2(s[nt][3] - mu1);
-      ps0 += s[nt][0] + s[nt][1];
-      ps1 += s[nt][2] + s[nt][3];
-    }
-    l0 = l0 * corr0 + ps0;
-    l1 = l1 * corr1 + ps1;
-    if (__any_sync(0xffffffffu, corr0 != 1.f || corr1 != 1.f)) {   // a row maximum moved
-#pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        o[n][0] *= corr0;
-        o[n][1] *= corr0;
-        o[n][2] *= corr1;
-        o[n][3] *= corr1;
+      for (int off = 4; off < 32; off <<= 1) {
+        r0 = fmaxf(r0, __shfl_xor_sync(0xffffffffu, r0, off));
+        r1 = fmaxf(r1, __shfl_xor_sync(0xffffffffu, r1, off));
       }
-    }
-    uint32_t pa[4];
-    pa[0] = pack2<F16>(s[0][0], s[0][1]);
-    pa[1] = pack2<F16>(s[0][2], s[0][3]);
-    pa[2] = pack2<F16>(s[1][0], s[1][1]);
-    pa[3] = pack2<F16>(s[1][2], s[1][3]);
-    // O += P V.
+      const float mn0 = fmaxf(m0, r0), mn1 = fmaxf(m1, r1);
+      const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+      const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float corr0 = ex2(m0 - mu0), corr1 = ex2(m1 - mu1);
+      m0 = mn0;
+      m1 = mn1;
+      v[0] = ex2(v[0] - mu0);
+      v[2] = ex2(v[2] - mu0);
+      v[1] = ex2(v[1] - mu1);
+      v[3] = ex2(v[3] - mu1);
+      l0 = l0 * corr0 + (v[0] + v[2]);
+      l1 = l1 * corr1 + (v[1] + v[3]);
+      if (__any_sync(0xffffffffu, corr0 != 1.f || corr1 != 1.f)) {
 #pragma unroll
-    for (int dp = 0; dp < D / 16; ++dp) {
-      const int r = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-      const int c = dp * 2 + (lane >> 4);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(smem_u32(tv + swz<D>(r, c)), b0, b1, b2, b3);
-      mma16816<F16>(o[2 * dp], pa, b0, b1);
-      mma16816<F16>(o[2 * dp + 1], pa, b2, b3);
+        for (int n = 0; n < kOB; ++n) {
+          o[n][0] *= corr0;
+          o[n][1] *= corr1;
+          o[n][2] *= corr0;
+          o[n][3] *= corr1;
+        }
+      }
+      // P^T as the B operand: lane (g, c4) wants keys 2c4, 2c4+1 (and +8) of
+      // head g, the transpose of what it holds.
+      const uint32_t pb0 = movm_t(pack2<F16>(v[0], v[1]));
+      const uint32_t pb1 = movm_t(pack2<F16>(v[2], v[3]));
+      // ---- O^T += V^T P^T ----
+      if constexpr (FP8) {
+        // Lane (g, c4) reads one word (dims 4w..4w+3, w = g + 8wg) of key rows
+        // 2c4, 2c4+1, 2c4+8, 2c4+9 and pairs the keys byte-wise: block 2wg
+        // carries dims 4w (row g) and 4w+1 (row g+8), block 2wg+1 dims 4w+2
+        // and 4w+3.  The output is un-permuted when it leaves the registers.
+        const int r0v = warp * 16 + 2 * c4;
+#pragma unroll
+        for (int wg = 0; wg < D / 32; ++wg) {
+          const int w = g + 8 * wg, c = w >> 2, wo = (w & 3) * 4;
+          const uint32_t x0 = *reinterpret_cast<const uint32_t *>(tv + vswz8<D>(r0v, c) + wo);
+          const uint32_t y0 = *reinterpret_cast<const uint32_t *>(tv + vswz8<D>(r0v + 1, c) + wo);
+          const uint32_t x1 = *reinterpret_cast<const uint32_t *>(tv + vswz8<D>(r0v + 8, c) + wo);
+          const uint32_t y1 = *reinterpret_cast<const uint32_t *>(tv + vswz8<D>(r0v + 9, c) + wo);
+          const uint32_t lo0 = __byte_perm(x0, y0, 0x5140), hi0 = __byte_perm(x0, y0, 0x7362);
+          const uint32_t lo1 = __byte_perm(x1, y1, 0x5140), hi1 = __byte_perm(x1, y1, 0x7362);
+          const uint32_t a0[4] = {e4m3x2_to_f16x2(lo0), e4m3x2_to_f16x2(lo0 >> 16),
+                                  e4m3x2_to_f16x2(lo1), e4m3x2_to_f16x2(lo1 >> 16)};
+          const uint32_t a1[4] = {e4m3x2_to_f16x2(hi0), e4m3x2_to_f16x2(hi0 >> 16),
+                                  e4m3x2_to_f16x2(hi1), e4m3x2_to_f16x2(hi1 >> 16)};
+          mma16816<true>(o[2 * wg], a0, pb0, pb1);
+          mma16816<true>(o[2 * wg + 1], a1, pb0, pb1);
+        }
+      } else {
+        const int vr = warp * 16 + (lane >> 4) * 8 + (lane & 7);
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          uint32_t a[4];
+          ldsm_x4_t(smem_u32(tv + swz<D>(vr, 2 * mt + ((lane >> 3) & 1))), a[0], a[1], a[2], a[3]);
+          mma16816<false>(o[mt], a, pb0, pb1);
+        }
+      }
+    } else {
+      // ---- S = Q K^T for this warp's 16 keys ----
+      // Two accumulators per 8-key block halve the dependent mma chain.
+      float s[2][4], sx[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[nt][e] = sx[nt][e] = 0.f;
+        const int r = warp * 16 + nt * 8 + (lane & 7);
+        if constexpr (FP8) {
+          // ldmatrix of raw E4M3 rows: register j holds 4 dims of chunk 4kq+j.
+#pragma unroll
+          for (int kq = 0; kq < D / 64; ++kq) {
+            uint32_t w[4];
+            ldsm_x4(smem_u32(st + kswz8<D>(r, kq * 4 + (lane >> 3))), w[0], w[1], w[2], w[3]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t lo = e4m3x2_to_f16x2(w[j]), hi = e4m3x2_to_f16x2(w[j] >> 16);
+              mma16816<true>((j & 1) ? sx[nt] : s[nt], qa[kq * 4 + j], lo, hi);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 32; ++kk) {
+            const int c = kk * 4 + (lane >> 3);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(smem_u32(st + swz<D>(r, c)), b0, b1, b2, b3);
+            mma16816<false>(s[nt], qa[2 * kk], b0, b1);
+            mma16816<false>(sx[nt], qa[2 * kk + 1], b2, b3);
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[nt][e] += sx[nt][e];
+      }
+      // Scale, mask, online softmax (rows g and g+8).
+      float rmax0 = -INFINITY, rmax1 = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int64_t j = kbase_j + nt * 8 + 2 * c4 + (e & 1);
+          float v = s[nt][e] * P.qk_scale_log2;
+          if (j >= k1) v = -INFINITY;
+          s[nt][e] = v;
+        }
+        rmax0 = fmaxf(rmax0, fmaxf(s[nt][0], s[nt][1]));
+        rmax1 = fmaxf(rmax1, fmaxf(s[nt][2], s[nt][3]));
+      }
+      rmax0 = fmaxf(rmax0, __shfl_xor_sync(0xffffffffu, rmax0, 1));
+      rmax0 = fmaxf(rmax0, __shfl_xor_sync(0xffffffffu, rmax0, 2));
+      rmax1 = fmaxf(rmax1, __shfl_xor_sync(0xffffffffu, rmax1, 1));
+      rmax1 = fmaxf(rmax1, __shfl_xor_sync(0xffffffffu, rmax1, 2));
+      const float mn0 = fmaxf(m0, rmax0), mn1 = fmaxf(m1, rmax1);
+      const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+      const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float corr0 = ex2(m0 - mu0), corr1 = ex2(m1 - mu1);
+      m0 = mn0;
+      m1 = mn1;
+      float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        s[nt][0] = ex2(s[nt][0] - mu0);
+        s[nt][1] = ex2(s[nt][1] - mu0);
+        s[nt][2] = ex2(s[nt][2] - mu1);
+        s[nt][3] = ex2(s[nt][3] - mu1);
+        ps0 += s[nt][0] + s[nt][1];
+        ps1 += s[nt][2] + s[nt][3];
+      }
+      l0 = l0 * corr0 + ps0;
+      l1 = l1 * corr1 + ps1;
+      if (__any_sync(0xffffffffu, corr0 != 1.f || corr1 != 1.f)) {   // a row maximum moved
+#pragma unroll
+        for (int n = 0; n < kOB; ++n) {
+          o[n][0] *= corr0;
+          o[n][1] *= corr0;
+          o[n][2] *= corr1;
+          o[n][3] *= corr1;
+        }
+      }
+      uint32_t pa[4];
+      pa[0] = pack2<F16>(s[0][0], s[0][1]);
+      pa[1] = pack2<F16>(s[0][2], s[0][3]);
+      pa[2] = pack2<F16>(s[1][0], s[1][1]);
+      pa[3] = pack2<F16>(s[1][2], s[1][3]);
+      // ---- O += P V ----
+      if constexpr (FP8) {
+        // Lane (g, c4) needs V at keys (2c4, 2c4+1) and (2c4+8, 2c4+9) for
+        // one output column per 8-column block: it reads one word (4 dims) of
+        // each of those four rows and pairs the keys byte-wise, so n-block
+        // 4ng+q carries dim 4(n + 8ng) + q at column n.  The output is
+        // un-permuted when it leaves the registers.
+        const int r0 = warp * 16 + 2 * c4;
+#pragma unroll
+        for (int ng = 0; ng < D / 32; ++ng) {
+          const int w = g + 8 * ng, c = w >> 2, wo = (w & 3) * 4;
+          const uint32_t a0 = *reinterpret_cast<const uint32_t *>(tv + vswz8<D>(r0, c) + wo);
+          const uint32_t b0 = *reinterpret_cast<const uint32_t *>(tv + vswz8<D>(r0 + 1, c) + wo);
+          const uint32_t a1 = *reinterpret_cast<const uint32_t *>(tv + vswz8<D>(r0 + 8, c) + wo);
+          const uint32_t b1 = *reinterpret_cast<const uint32_t *>(tv + vswz8<D>(r0 + 9, c) + wo);
+          const uint32_t lo0 = __byte_perm(a0, b0, 0x5140), hi0 = __byte_perm(a0, b0, 0x7362);
+          const uint32_t lo1 = __byte_perm(a1, b1, 0x5140), hi1 = __byte_perm(a1, b1, 0x7362);
+          mma16816<true>(o[4 * ng + 0], pa, e4m3x2_to_f16x2(lo0), e4m3x2_to_f16x2(lo1));
+          mma16816<true>(o[4 * ng + 1], pa, e4m3x2_to_f16x2(lo0 >> 16), e4m3x2_to_f16x2(lo1 >> 16));
+          mma16816<true>(o[4 * ng + 2], pa, e4m3x2_to_f16x2(hi0), e4m3x2_to_f16x2(hi1));
+          mma16816<true>(o[4 * ng + 3], pa, e4m3x2_to_f16x2(hi0 >> 16), e4m3x2_to_f16x2(hi1 >> 16));
+        }
+      } else {
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {
+          const int r = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+          const int c = dp * 2 + (lane >> 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(smem_u32(tv + swz<D>(r, c)), b0, b1, b2, b3);
+          mma16816<false>(o[2 * dp], pa, b0, b1);
+          mma16816<false>(o[2 * dp + 1], pa, b2, b3);
+        }
+      }
     }
   }
   cp_wait<0>();
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  if constexpr (KM) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+  } else {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  }
   __syncthreads();  // stages no longer needed: reuse for the warp merge
 
   constexpr int OS = D + 4;
   float *sm_o = reinterpret_cast<float *>(smem);
   float *sm_m = sm_o + kWarps * 16 * OS;
   float *sm_l = sm_m + kWarps * 16;
-  if (c4 == 0) {
-    sm_m[warp * 16 + g] = m0;
-    sm_m[warp * 16 + g + 8] = m1;
-    sm_l[warp * 16 + g] = l0;
-    sm_l[warp * 16 + g + 8] = l1;
-  }
+  if constexpr (KM) {
+    if (g == 0) {
+      sm_m[warp * 16 + 2 * c4] = m0;
+      sm_m[warp * 16 + 2 * c4 + 1] = m1;
+      sm_l[warp * 16 + 2 * c4] = l0;
+      sm_l[warp * 16 + 2 * c4 + 1] = l1;
+    }
+    float *h0p = sm_o + (warp * 16 + 2 * c4) * OS;
+    float *h1p = h0p + OS;
 #pragma unroll
-  for (int n = 0; n < D / 8; ++n) {
-    float *r0p = sm_o + (warp * 16 + g) * OS + n * 8 + 2 * c4;
-    float *r1p = sm_o + (warp * 16 + g + 8) * OS + n * 8 + 2 * c4;
-    r0p[0] = o[n][0];
-    r0p[1] = o[n][1];
-    r1p[0] = o[n][2];
-    r1p[1] = o[n][3];
+    for (int mt = 0; mt < D / 16; ++mt) {
+      // Dims of accumulator rows g and g+8 (FP8: as the V pairing gave them).
+      const int da = FP8 ? 4 * (g + 8 * (mt >> 1)) + 2 * (mt & 1) : mt * 16 + g;
+      const int db = FP8 ? da + 1 : da + 8;
+      h0p[da] = o[mt][0];
+      h1p[da] = o[mt][1];
+      h0p[db] = o[mt][2];
+      h1p[db] = o[mt][3];
+    }
+  } else {
+    if (c4 == 0) {
+      sm_m[warp * 16 + g] = m0;
+      sm_m[warp * 16 + g + 8] = m1;
+      sm_l[warp * 16 + g] = l0;
+      sm_l[warp * 16 + g + 8] = l1;
+    }
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      // Columns of accumulator block n (FP8: the dims the V pairing gave them).
+      const int d0 = FP8 ? 4 * (2 * c4 + 8 * (n >> 2)) + (n & 3) : n * 8 + 2 * c4;
+      const int d1 = FP8 ? d0 + 4 : d0 + 1;
+      float *r0p = sm_o + (warp * 16 + g) * OS;
+      float *r1p = sm_o + (warp * 16 + g + 8) * OS;
+      r0p[d0] = o[n][0];
+      r0p[d1] = o[n][1];
+      r1p[d0] = o[n][2];
+      r1p[d1] = o[n][3];
+    }
   }
   __syncthreads();
 
@@ -485,8 +702,7 @@ Layout layout_of(const Ctx &c, int layer, int64_t nq, int max_seq_len) {
   const LayerInfo &L = c.layers[layer];
   const int G = c.cfg.num_q_heads / L.hkv;
   const int mk = max_keys_of(c, layer, max_seq_len);
-  w.split_keys = decode_split_keys(c.num_sms, nq, L.hkv, mk, c.cfg.page_size,
-                                   c.cfg.head_dim * (c.cfg.kv_dtype == SWA_DTYPE_E4M3 ? 1 : 2));
+  w.split_keys = decode_split_keys(c.num_sms, nq, L.hkv, mk, c.cfg.page_size);
   w.max_splits = (mk + w.split_keys - 1) / w.split_keys;
   size_t part = (size_t)nq * L.hkv * w.max_splits * part_stride(G, c.cfg.head_dim) * sizeof(float);
   w.ticket_off = 256 + (part + 255) / 256 * 256;   // first 256 bytes: reserved counters
@@ -494,14 +710,14 @@ Layout layout_of(const Ctx &c, int layer, int64_t nq, int max_seq_len) {
   return w;
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool KM>
 cudaError_t launch_t(dim3 grid, const MmaParams &P, cudaStream_t s) {
   // Main tiles (or merge scratch), then the split's page-row table.
-  const int smem = Smem<D, FP8>::kTotal + (P.split_keys / P.ps + 2) * (int)sizeof(int64_t);
-  cudaError_t e = cudaFuncSetAttribute(k_decode_mma<D, FP8>,
+  const int smem = Smem<D, FP8, KM>::kTotal + (P.split_keys / P.ps + 2) * (int)sizeof(int64_t);
+  cudaError_t e = cudaFuncSetAttribute(k_decode_mma<D, FP8, KM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k_decode_mma<D, FP8><<<grid, kWarps * 32, smem, s>>>(P);
+  k_decode_mma<D, FP8, KM><<<grid, kWarps * 32, smem, s>>>(P);
   return cudaGetLastError();
 }
 
@@ -549,8 +765,12 @@ cudaError_t launch_attn_decode_mma(Ctx &c, const AttnArgs &a, cudaStream_t s) {
   P.err = c.err_word;
   dim3 grid(L.hkv, w.max_splits, a.nq);
   const int D = c.cfg.head_dim;
-  if (D == 128) return fp8 ? launch_t<128, true>(grid, P, s) : launch_t<128, false>(grid, P, s);
-  return fp8 ? launch_t<64, true>(grid, P, s) : launch_t<64, false>(grid, P, s);
+  if (P.G <= 8) {   // keys as rows
+    if (D == 128) return fp8 ? launch_t<128, true, true>(grid, P, s) : launch_t<128, false, true>(grid, P, s);
+    return fp8 ? launch_t<64, true, true>(grid, P, s) : launch_t<64, false, true>(grid, P, s);
+  }
+  if (D == 128) return fp8 ? launch_t<128, true, false>(grid, P, s) : launch_t<128, false, false>(grid, P, s);
+  return fp8 ? launch_t<64, true, false>(grid, P, s) : launch_t<64, false, false>(grid, P, s);
 }
 
 }  // namespace swa

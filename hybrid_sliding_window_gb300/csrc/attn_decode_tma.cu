@@ -668,8 +668,7 @@ static WsLayout ws_layout(const Ctx &c, int layer, int64_t nq, int max_seq_len) 
   const int G = c.cfg.num_q_heads / L.hkv;
   const int mk = max_keys_of(c, layer, max_seq_len);
   WsLayout w;
-  w.split_keys = decode_split_keys(c.num_sms, nq, L.hkv, mk, c.cfg.page_size,
-                                   c.cfg.head_dim * (c.cfg.kv_dtype == SWA_DTYPE_E4M3 ? 1 : 2));
+  w.split_keys = decode_split_keys(c.num_sms, nq, L.hkv, mk, c.cfg.page_size);
   if (w.split_keys > kMaxSplitKeys) w.split_keys = kMaxSplitKeys;
   w.max_splits = (mk + w.split_keys - 1) / w.split_keys;
   const size_t part = (size_t)nq * L.hkv * w.max_splits * part_stride(G, c.cfg.head_dim) * sizeof(float);

@@ -23,16 +23,16 @@ __host__ __device__ inline int part_stride(int G, int D) { return (G * D + 2 * G
 // of the key stream; each costs a fixed prologue (page rows, first tiles in
 // flight) and epilogue (warp merge, partial write, ticket) of several
 // microseconds, so long splits pay less; but the last splits to start set the
-// tail, so they must stay short against the per-SM share of the work.
-// Measured on the decode workloads: 4096 keys is best for 256-byte head rows
-// (a bf16 row of 128), 2048 for 128-byte rows.  Fewer than two splits per SM
-// slot (2 CTAs per SM, counted for a mean of half the longest request) halve
-// it, down to 1024 keys; at most 512 pages per split (the page-row table
-// lives in shared memory).
-inline int decode_split_keys(int num_sms, int64_t nq, int hkv, int64_t max_keys, int ps,
-                             int row_bytes) {
+// tail, so they must stay short against the per-SM share of the work.  Only
+// the batch and the longest request are known on the host: the longest
+// request gets about eight splits (a power of two from 1024 to 4096 keys),
+// halved while there are fewer than two splits per SM slot (2 CTAs per SM,
+// counted for a mean of half the longest request), down to 1024; at most 512
+// pages per split (the page-row table lives in shared memory).
+inline int decode_split_keys(int num_sms, int64_t nq, int hkv, int64_t max_keys, int ps) {
   const int64_t slots = 2LL * (num_sms > 0 ? num_sms : 148);
-  int split = row_bytes >= 256 ? 4096 : 2048;
+  int split = 1024;
+  while (split < 4096 && split * 8LL < max_keys) split *= 2;
   while (split > 1024 && nq * hkv * ((max_keys / 2 + split - 1) / split) < 2 * slots) split /= 2;
   return split < 512 * ps ? split : 512 * ps;
 }
