@@ -260,16 +260,7 @@ def run_native(args, rank, world):
     peak, peak_kind = peaks()
     value = tot_bytes / (t_ms_max / 1e3) / 1e9
     ach = (sum(attn_bytes) / len(attn_bytes)) / (full_attn_ms / 1e3) / 1e9
-    traffic = None
-    tp = os.path.join(ROOT, "profiles", f"{args.workload}_decode_traffic.json")
-    if os.path.exists(tp):
-        try:
-            with open(tp) as f:
-                tj = json.load(f)
-            if tj.get("kernel_source_hash") == kernel_hash():
-                traffic = tj["bytes_per_launch"]
-        except Exception:
-            traffic = None
+    traffic = stored_traffic(f"{args.workload}_decode_traffic.json", DECODE_SOURCES)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(t_ms_max / K, 4),
@@ -401,7 +392,8 @@ def run_extend(args, rank, world, quiet=False):
                    "l2": "no flush: each round reads ~1.3 GB of KV per full layer pass"},
         "frac_of_sustained_bf16": round(flops["total"] / (t_ms / 1e3) / 1e12 / sustained, 4),
         "roofline": {"bound": "tensor", "achieved": round(ach, 1), "peak": burst,
-                     "unit": "TFLOP/s", "frac": round(ach / burst, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(ach / burst, 4),
+                     "traffic": stored_traffic("extend_traffic.json", EXTEND_SOURCES),
                      "kernel": "swa_attn_extend on full layers (tcgen05)",
                      "peak_source": src, "avg_launch_ms": round(full_ms, 3)},
         "full_round_ms": round(round_ms, 3),
@@ -412,15 +404,35 @@ def run_extend(args, rank, world, quiet=False):
     }
 
 
-def kernel_hash():
+# Sources of the dominant kernel of each bench line: its DRAM traffic, taken
+# from an ncu capture and stored under profiles/, is reported only while
+# these files are unchanged since the capture.
+DECODE_SOURCES = ("attn_decode_mma.cu", "split_merge.cuh", "swa_internal.h")
+EXTEND_SOURCES = ("attn_extend_tc.cu", "swa_internal.h")
+
+
+def kernel_hash(files):
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "hybrid_sliding_window_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".h")):
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(fh.read())
+    for f in files:
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def stored_traffic(name, files):
+    """DRAM bytes (read + write) per launch from a stored ncu summary, or None
+    when the kernel's sources changed since it was taken."""
+    tp = os.path.join(ROOT, "profiles", name)
+    try:
+        with open(tp) as f:
+            tj = json.load(f)
+        if tj.get("kernel_source_hash") == kernel_hash(files):
+            return tj["bytes_per_launch"]
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
 
 
 # ------------------------------------------------------------- reference ---

@@ -165,10 +165,13 @@ __device__ __forceinline__ int vswz8(int r, int c) {
   return r * D + ((c ^ (D == 128 ? 2 * ((r >> 1) & 3) : 2 * ((r >> 1) & 1))) << 4);
 }
 
-// Two E4M3 values (low byte first) to an f16 pair; exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v & 0xffffu), __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// Four E4M3 values (bytes 0..3 of w) to two f16 pairs, (b0, b1) and (b2, b3),
+// low byte in the low half; exact (E4M3 is a subset of f16).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 // Transpose of an 8x8 16-bit block held one row-pair per lane.
@@ -368,10 +371,11 @@ __global__ void __launch_bounds__(kWarps * 32, (Smem<D, FP8, KM>::kMinBlocks))
         for (int kp = 0; kp < D / 32; ++kp) {   // two 16-dim steps per ldmatrix
           uint32_t w[4];
           ldsm_x4(smem_u32(st + kswz8<D>(kr, 2 * kp + (lane >> 4))), w[0], w[1], w[2], w[3]);
-          const uint32_t a0[4] = {e4m3x2_to_f16x2(w[0]), e4m3x2_to_f16x2(w[1]),
-                                  e4m3x2_to_f16x2(w[0] >> 16), e4m3x2_to_f16x2(w[1] >> 16)};
-          const uint32_t a1[4] = {e4m3x2_to_f16x2(w[2]), e4m3x2_to_f16x2(w[3]),
-                                  e4m3x2_to_f16x2(w[2] >> 16), e4m3x2_to_f16x2(w[3] >> 16)};
+          uint32_t a0[4], a1[4];
+          e4m3x4_to_f16x2x2(w[0], a0[0], a0[2]);
+          e4m3x4_to_f16x2x2(w[1], a0[1], a0[3]);
+          e4m3x4_to_f16x2x2(w[2], a1[0], a1[2]);
+          e4m3x4_to_f16x2x2(w[3], a1[1], a1[3]);
           mma16816<true>(sa, a0, qa[2 * kp][0], qa[2 * kp][1]);
           mma16816<true>(sb, a1, qa[2 * kp + 1][0], qa[2 * kp + 1][1]);
         }
@@ -437,10 +441,11 @@ __global__ void __launch_bounds__(kWarps * 32, (Smem<D, FP8, KM>::kMinBlocks))
           const uint32_t y1 = *reinterpret_cast<const uint32_t *>(tv + vswz8<D>(r0v + 9, c) + wo);
           const uint32_t lo0 = __byte_perm(x0, y0, 0x5140), hi0 = __byte_perm(x0, y0, 0x7362);
           const uint32_t lo1 = __byte_perm(x1, y1, 0x5140), hi1 = __byte_perm(x1, y1, 0x7362);
-          const uint32_t a0[4] = {e4m3x2_to_f16x2(lo0), e4m3x2_to_f16x2(lo0 >> 16),
-                                  e4m3x2_to_f16x2(lo1), e4m3x2_to_f16x2(lo1 >> 16)};
-          const uint32_t a1[4] = {e4m3x2_to_f16x2(hi0), e4m3x2_to_f16x2(hi0 >> 16),
-                                  e4m3x2_to_f16x2(hi1), e4m3x2_to_f16x2(hi1 >> 16)};
+          uint32_t a0[4], a1[4];
+          e4m3x4_to_f16x2x2(lo0, a0[0], a0[1]);
+          e4m3x4_to_f16x2x2(lo1, a0[2], a0[3]);
+          e4m3x4_to_f16x2x2(hi0, a1[0], a1[1]);
+          e4m3x4_to_f16x2x2(hi1, a1[2], a1[3]);
           mma16816<true>(o[2 * wg], a0, pb0, pb1);
           mma16816<true>(o[2 * wg + 1], a1, pb0, pb1);
         }
@@ -470,7 +475,8 @@ __global__ void __launch_bounds__(kWarps * 32, (Smem<D, FP8, KM>::kMinBlocks))
             ldsm_x4(smem_u32(st + kswz8<D>(r, kq * 4 + (lane >> 3))), w[0], w[1], w[2], w[3]);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const uint32_t lo = e4m3x2_to_f16x2(w[j]), hi = e4m3x2_to_f16x2(w[j] >> 16);
+              uint32_t lo, hi;
+              e4m3x4_to_f16x2x2(w[j], lo, hi);
               mma16816<true>((j & 1) ? sx[nt] : s[nt], qa[kq * 4 + j], lo, hi);
             }
           }
@@ -554,10 +560,15 @@ __global__ void __launch_bounds__(kWarps * 32, (Smem<D, FP8, KM>::kMinBlocks))
           const uint32_t b1 = *reinterpret_cast<const uint32_t *>(tv + vswz8<D>(r0 + 9, c) + wo);
           const uint32_t lo0 = __byte_perm(a0, b0, 0x5140), hi0 = __byte_perm(a0, b0, 0x7362);
           const uint32_t lo1 = __byte_perm(a1, b1, 0x5140), hi1 = __byte_perm(a1, b1, 0x7362);
-          mma16816<true>(o[4 * ng + 0], pa, e4m3x2_to_f16x2(lo0), e4m3x2_to_f16x2(lo1));
-          mma16816<true>(o[4 * ng + 1], pa, e4m3x2_to_f16x2(lo0 >> 16), e4m3x2_to_f16x2(lo1 >> 16));
-          mma16816<true>(o[4 * ng + 2], pa, e4m3x2_to_f16x2(hi0), e4m3x2_to_f16x2(hi1));
-          mma16816<true>(o[4 * ng + 3], pa, e4m3x2_to_f16x2(hi0 >> 16), e4m3x2_to_f16x2(hi1 >> 16));
+          uint32_t l0a, l0b, l1a, l1b, h0a, h0b, h1a, h1b;
+          e4m3x4_to_f16x2x2(lo0, l0a, l0b);
+          e4m3x4_to_f16x2x2(lo1, l1a, l1b);
+          e4m3x4_to_f16x2x2(hi0, h0a, h0b);
+          e4m3x4_to_f16x2x2(hi1, h1a, h1b);
+          mma16816<true>(o[4 * ng + 0], pa, l0a, l1a);
+          mma16816<true>(o[4 * ng + 1], pa, l0b, l1b);
+          mma16816<true>(o[4 * ng + 2], pa, h0a, h1a);
+          mma16816<true>(o[4 * ng + 3], pa, h0b, h1b);
         }
       } else {
 #pragma unroll
