@@ -31,8 +31,6 @@
 namespace swa {
 namespace {
 
-constexpr int kTile = 64;
-constexpr int kWarps = 4;
 
 struct MmaParams {
   int kind, window, hkv, G, ps;
@@ -115,11 +113,31 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
-__device__ __forceinline__ int64_t key_slot(const MmaParams &P, int b, int64_t j) {
-  if (P.kind == SWA_LAYER_FULL) return P.rt[P.req_idx[b] * P.rt_stride + j];
-  const int32_t *h = P.plan.hdr + b * 4;
-  const int64_t k = j / P.ps - h[2];
-  if (j < h[0] || k < 0 || k >= h[3]) {
+// Per-request table entry points, read once at the start of a CTA (they do
+// not depend on the sequence length, so their loads overlap with it): the
+// req_to_token row of a full layer, the plan header of a windowed one.
+struct ReqRef {
+  int64_t row;           // full: req_idx[b]
+  int32_t h0, h2, h3;    // windowed: first planned position, first page, page count
+};
+
+__device__ __forceinline__ ReqRef req_ref(const MmaParams &P, int b) {
+  ReqRef r{0, 0, 0, 0};
+  if (P.kind == SWA_LAYER_FULL) {
+    r.row = P.req_idx[b];
+  } else {
+    const int32_t *h = P.plan.hdr + b * 4;
+    r.h0 = h[0];
+    r.h2 = h[2];
+    r.h3 = h[3];
+  }
+  return r;
+}
+
+__device__ __forceinline__ int64_t key_slot(const MmaParams &P, const ReqRef &R, int b, int64_t j) {
+  if (P.kind == SWA_LAYER_FULL) return P.rt[R.row * P.rt_stride + j];
+  const int64_t k = j / P.ps - R.h2;
+  if (j < R.h0 || k < 0 || k >= R.h3) {
     set_error(P.err, SWA_DEVERR_RANGE);
     return 0;
   }
@@ -134,16 +152,20 @@ __device__ __forceinline__ int64_t key_slot(const MmaParams &P, int b, int64_t j
 // Heads-as-rows (G > 8) FP8 stages are half the size of bf16 ones, so twice
 // as many fit at 2 CTAs per SM; keys-as-rows kernels need fewer registers and
 // run 4 CTAs per SM where the tiles allow.
-template <int D, bool FP8, bool KM>
+template <int D, bool FP8, bool KM, int NW>
 struct Smem {
+  static constexpr int kWarps = NW;
+  static constexpr int kTile = 16 * NW;   // keys per stage: 16 per warp
   static constexpr int kEsz = FP8 ? 1 : 2;
   static constexpr int kStages = (FP8 && !KM) ? 6 : 3;
   static constexpr int kQ = 16 * D * 2;
   static constexpr int kStageBytes = 2 * kTile * D * kEsz;
   static constexpr int kMerge = kWarps * 16 * (D + 4) * 4 + 2 * kWarps * 16 * 4;
   static constexpr int kMain = kQ + kStages * kStageBytes;
-  static constexpr int kTotal = kMain > kMerge ? kMain : kMerge;
-  static constexpr int kMinBlocks = (D == 64 || (KM && FP8)) ? 4 : 2;
+  static constexpr int kBig = kMain > kMerge ? kMain : kMerge;
+  static constexpr int kTotal = kBig > kMergeScratchBytes ? kBig : kMergeScratchBytes;
+  static constexpr int kMinBlocks =
+      NW == 2 ? (D == 64 ? 8 : 4) : ((D == 64 || (KM && FP8)) ? 4 : 2);
 };
 
 // 16-bit tile addressing: row r, 16-byte chunk c (D/8 chunks per row), XOR swizzle.
@@ -193,10 +215,12 @@ struct CtaSync {
 //    the heads as N = 8, then O^T += V^T P^T, P^T transposed in registers.
 //    Half the tensor-core work when the group has at most 8 heads, and half
 //    the accumulator registers.
-template <int D, bool FP8, bool KM>
-__global__ void __launch_bounds__(kWarps * 32, (Smem<D, FP8, KM>::kMinBlocks))
+template <int D, bool FP8, bool KM, int NW>
+__global__ void __launch_bounds__(NW * 32, (Smem<D, FP8, KM, NW>::kMinBlocks))
     k_decode_mma(MmaParams P) {
-  using S = Smem<D, FP8, KM>;
+  using S = Smem<D, FP8, KM, NW>;
+  constexpr int kWarps = NW;
+  constexpr int kTile = S::kTile;
   static_assert(S::kTotal >= kMergeScratchBytes, "merge scratch exceeds the tiles");
   constexpr bool F16 = FP8;                 // FP8 KV widens to f16; bf16 KV stays bf16
   constexpr int kStages = S::kStages;
@@ -208,23 +232,15 @@ __global__ void __launch_bounds__(kWarps * 32, (Smem<D, FP8, KM>::kMinBlocks))
 
   // KV heads fastest: the CTAs of all heads of the same keys run together, so
   // each token's interleaved head rows are read from DRAM at about one time.
-  const int kvh = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
+  // Split index slowest: every request's leading (full-length) splits are
+  // dispatched first and the last wave holds the ragged final splits of the
+  // longest requests, which shortens the tail.
+  const int kvh = blockIdx.x, b = blockIdx.y, split = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = P.G;
   const int Hq = P.hkv * G;
 
-  // ---- Q rows into registers first: their latency hides behind the
-  // page-row lookups and the first tile loads ----
-  constexpr int kQPer = 16 * (D / 8) / (kWarps * 32);
-  uint4 qv[kQPer];
-#pragma unroll
-  for (int k = 0; k < kQPer; ++k) {
-    const int i = tid + k * kWarps * 32;
-    const int r = i / (D / 8), c = i % (D / 8);
-    qv[k] = make_uint4(0, 0, 0, 0);
-    if (r < G) qv[k] = *reinterpret_cast<const uint4 *>(P.q + ((int64_t)b * Hq + kvh * G + r) * D + c * 8);
-  }
-
+  const ReqRef R = req_ref(P, b);
   const int64_t p = P.seq[b] - 1;
   int64_t lo = 0;
   if (P.kind == SWA_LAYER_SLIDING) lo = p - P.window > 0 ? p - P.window : 0;
@@ -236,6 +252,18 @@ __global__ void __launch_bounds__(kWarps * 32, (Smem<D, FP8, KM>::kMinBlocks))
   const int64_t k1 = min(p + 1, k0 + P.split_keys);
   const int n_tiles = (int)((k1 - k0 + kTile - 1) / kTile);
 
+  // ---- Q rows into registers: their latency hides behind the page-row
+  // lookups and the first tile loads ----
+  constexpr int kQPer = 16 * (D / 8) / (kWarps * 32);
+  uint4 qv[kQPer];
+#pragma unroll
+  for (int k = 0; k < kQPer; ++k) {
+    const int i = tid + k * kWarps * 32;
+    const int r = i / (D / 8), c = i % (D / 8);
+    qv[k] = make_uint4(0, 0, 0, 0);
+    if (r < G) qv[k] = *reinterpret_cast<const uint4 *>(P.q + ((int64_t)b * Hq + kvh * G + r) * D + c * 8);
+  }
+
   // ---- page rows of this split, looked up once (one table read per page) ----
   // Positions of one page occupy consecutive slots of one pool page, so the
   // row of key j is rowbase[j / ps - pg0] + j % ps.
@@ -246,7 +274,7 @@ __global__ void __launch_bounds__(kWarps * 32, (Smem<D, FP8, KM>::kMinBlocks))
   const int64_t max_page = (P.pool_rows / P.ps) - 1;
   for (int i = tid; i < n_pg; i += blockDim.x) {
     const int64_t pos = (pg0 + i) * P.ps > k0 ? (pg0 + i) * P.ps : k0;
-    const int64_t slot = key_slot(P, b, pos);
+    const int64_t slot = key_slot(P, R, b, pos);
     int64_t page = slot / P.ps;
     if (slot < 0 || page > max_page) {
       set_error(P.err, SWA_DEVERR_RANGE);
@@ -721,14 +749,14 @@ Layout layout_of(const Ctx &c, int layer, int64_t nq, int max_seq_len) {
   return w;
 }
 
-template <int D, bool FP8, bool KM>
+template <int D, bool FP8, bool KM, int NW = 4>
 cudaError_t launch_t(dim3 grid, const MmaParams &P, cudaStream_t s) {
   // Main tiles (or merge scratch), then the split's page-row table.
-  const int smem = Smem<D, FP8, KM>::kTotal + (P.split_keys / P.ps + 2) * (int)sizeof(int64_t);
-  cudaError_t e = cudaFuncSetAttribute(k_decode_mma<D, FP8, KM>,
+  const int smem = Smem<D, FP8, KM, NW>::kTotal + (P.split_keys / P.ps + 2) * (int)sizeof(int64_t);
+  cudaError_t e = cudaFuncSetAttribute(k_decode_mma<D, FP8, KM, NW>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k_decode_mma<D, FP8, KM><<<grid, kWarps * 32, smem, s>>>(P);
+  k_decode_mma<D, FP8, KM, NW><<<grid, NW * 32, smem, s>>>(P);
   return cudaGetLastError();
 }
 
@@ -774,8 +802,15 @@ cudaError_t launch_attn_decode_mma(Ctx &c, const AttnArgs &a, cudaStream_t s) {
   P.max_splits = w.max_splits;
   P.split_keys = w.split_keys;
   P.err = c.err_word;
-  dim3 grid(L.hkv, w.max_splits, a.nq);
+  if (w.max_splits > 65535) return cudaErrorInvalidConfiguration;   // grid z limit
+  dim3 grid(L.hkv, a.nq, w.max_splits);
   const int D = c.cfg.head_dim;
+  if (P.G <= 8 && max_keys_of(c, a.layer, a.max_seq_len) <= 512) {
+    // Short streams (sliding windows): two warps on 32-key stages, so that
+    // more CTAs fit per SM and a whole layer runs in about one wave.
+    if (D == 128) return fp8 ? launch_t<128, true, true, 2>(grid, P, s) : launch_t<128, false, true, 2>(grid, P, s);
+    return fp8 ? launch_t<64, true, true, 2>(grid, P, s) : launch_t<64, false, true, 2>(grid, P, s);
+  }
   if (P.G <= 8) {   // keys as rows
     if (D == 128) return fp8 ? launch_t<128, true, true>(grid, P, s) : launch_t<128, false, true>(grid, P, s);
     return fp8 ? launch_t<64, true, true>(grid, P, s) : launch_t<64, false, true>(grid, P, s);
