@@ -190,6 +190,32 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
 }
+// Paired fp32 arithmetic (one instruction for two lanes of values) and a
+// three-input maximum: the softmax warps are bound by instruction issue, so
+// halving the instructions per score element is what speeds them up.
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};\n" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t r, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;\n" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
 // (row r, 16-byte chunk c in 0..15) of a 128 x 128 bf16 tile stored as two
@@ -445,11 +471,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         TC_LD32(tS + cb * 64 + 32, (rr + 32));
         tc_wait_ld();
         if (!masked) {
-          // four independent chains keep the FMNMX latency off the critical path
+          // four independent chains of three-input maxima
           float m2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int e = 0; e < 64; ++e) m2[e & 3] = fmaxf(m2[e & 3], __uint_as_float(rr[e]));
-          mx = fmaxf(mx, fmaxf(fmaxf(m2[0], m2[1]), fmaxf(m2[2], m2[3])));
+          for (int e = 0; e < 64; e += 2)
+            m2[(e >> 1) & 3] = max3(m2[(e >> 1) & 3], __uint_as_float(rr[e]), __uint_as_float(rr[e + 1]));
+          mx = max3(mx, max3(m2[0], m2[1], m2[2]), m2[3]);
         } else {
 #pragma unroll
           for (int e = 0; e < 64; ++e) {
@@ -482,7 +509,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sc = P.scale_log2;
       // Pass 2: P = exp2(scale*s - m) as packed bf16 pairs, written over the S
       // columns already consumed (64-key half cb -> columns [32 cb, 32 cb + 32)).
-      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint64_t sc2 = f2pack(sc, sc), nmu2 = f2pack(-mu, -mu);
+      uint64_t acc2[2] = {0ull, 0ull};   // running pair sums (two chains)
 #pragma unroll
       for (int cb = 0; cb < 2; ++cb) {
         uint32_t lo[32], hi[32];
@@ -494,20 +522,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 32; ++e) {
           const uint32_t x0 = e < 16 ? lo[2 * e] : hi[2 * e - 32];
           const uint32_t x1 = e < 16 ? lo[2 * e + 1] : hi[2 * e - 31];
-          float a0 = ex2(fmaf(__uint_as_float(x0), sc, -mu));
-          float a1 = ex2(fmaf(__uint_as_float(x1), sc, -mu));
+          float t0, t1;
+          f2unpack(fma2(f2pack(__uint_as_float(x0), __uint_as_float(x1)), sc2, nmu2), t0, t1);
+          float a0 = ex2(t0);
+          float a1 = ex2(t1);
           if (masked) {
             const int k0 = cb * 64 + 2 * e;
             if (k0 < e_lo || k0 > e_hi) a0 = 0.f;
             if (k0 + 1 < e_lo || k0 + 1 > e_hi) a1 = 0.f;
           }
-          ps4[e & 3] += a0 + a1;
+          acc2[e & 1] = add2(acc2[e & 1], f2pack(a0, a1));
           __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
           pk[e] = *reinterpret_cast<uint32_t *>(&h);
         }
         TC_ST32(tS + cb * 32, pk);
       }
-      l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+      {
+        float s0, s1, s2, s3;
+        f2unpack(acc2[0], s0, s1);
+        f2unpack(acc2[1], s2, s3);
+        l_run += (s0 + s1) + (s2 + s3);
+      }
       tc_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_PREADY + grp));
