@@ -462,28 +462,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Interior tiles (no row of the warp at a window or causal edge) skip
       // the per-key masks entirely.
       const bool masked = __any_sync(0xffffffffu, edge);
-      // Pass 1: row maximum (S is read from TMEM twice instead of held in registers).
-      float mx = -INFINITY;
+      // Keys outside this row's range read as -inf (edge tiles only): the
+      // max and the exponentials below then need no per-key test.
+      auto mask_in_place = [&](uint32_t (&rr)[64], int cb) {
 #pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          const int ee = cb * 64 + e;
+          if (ee < e_lo || ee > e_hi) rr[e] = 0xff800000u;   // -inf
+        }
+      };
+      // Pass 1: row maximum (S is read from TMEM twice instead of held in
+      // registers).  The 64-key loops stay rolled: one copy of each body
+      // keeps the softmax code inside the instruction cache.
+      float mx = -INFINITY;
+#pragma unroll 1
       for (int cb = 0; cb < kKeys / 64; ++cb) {
         uint32_t rr[64];
         TC_LD32(tS + cb * 64, rr);        // two loads in flight before one wait
         TC_LD32(tS + cb * 64 + 32, (rr + 32));
         tc_wait_ld();
-        if (!masked) {
-          // four independent chains of three-input maxima
-          float m2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (masked) mask_in_place(rr, cb);
+        // four independent chains of three-input maxima
+        float m2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int e = 0; e < 64; e += 2)
-            m2[(e >> 1) & 3] = max3(m2[(e >> 1) & 3], __uint_as_float(rr[e]), __uint_as_float(rr[e + 1]));
-          mx = max3(mx, max3(m2[0], m2[1], m2[2]), m2[3]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            const int ee = cb * 64 + e;
-            if (ee >= e_lo && ee <= e_hi) mx = fmaxf(mx, __uint_as_float(rr[e]));
-          }
-        }
+        for (int e = 0; e < 64; e += 2)
+          m2[(e >> 1) & 3] = max3(m2[(e >> 1) & 3], __uint_as_float(rr[e]), __uint_as_float(rr[e + 1]));
+        mx = max3(mx, max3(m2[0], m2[1], m2[2]), m2[3]);
       }
       mx = mx == -INFINITY ? -INFINITY : mx * P.scale_log2;
       // Lazy rescale: move the reference maximum only when it grows by more
@@ -494,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_run = mx;
       }
       if (t > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-#pragma unroll
+#pragma unroll 1
         for (int cb = 0; cb < kD / 32; ++cb) {
           uint32_t rr[32];
           TC_LD32(tO + cb * 32, rr);
@@ -511,26 +515,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // columns already consumed (64-key half cb -> columns [32 cb, 32 cb + 32)).
       const uint64_t sc2 = f2pack(sc, sc), nmu2 = f2pack(-mu, -mu);
       uint64_t acc2[2] = {0ull, 0ull};   // running pair sums (two chains)
-#pragma unroll
+#pragma unroll 1
       for (int cb = 0; cb < 2; ++cb) {
-        uint32_t lo[32], hi[32];
-        TC_LD32(tS + cb * 64, lo);
-        TC_LD32(tS + cb * 64 + 32, hi);
+        uint32_t rr[64];
+        TC_LD32(tS + cb * 64, rr);
+        TC_LD32(tS + cb * 64 + 32, (rr + 32));
         tc_wait_ld();
+        if (masked) mask_in_place(rr, cb);
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const uint32_t x0 = e < 16 ? lo[2 * e] : hi[2 * e - 32];
-          const uint32_t x1 = e < 16 ? lo[2 * e + 1] : hi[2 * e - 31];
           float t0, t1;
-          f2unpack(fma2(f2pack(__uint_as_float(x0), __uint_as_float(x1)), sc2, nmu2), t0, t1);
-          float a0 = ex2(t0);
-          float a1 = ex2(t1);
-          if (masked) {
-            const int k0 = cb * 64 + 2 * e;
-            if (k0 < e_lo || k0 > e_hi) a0 = 0.f;
-            if (k0 + 1 < e_lo || k0 + 1 > e_hi) a1 = 0.f;
-          }
+          f2unpack(fma2(f2pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1])), sc2, nmu2),
+                   t0, t1);
+          const float a0 = ex2(t0);
+          const float a1 = ex2(t1);
           acc2[e & 1] = add2(acc2[e & 1], f2pack(a0, a1));
           __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
           pk[e] = *reinterpret_cast<uint32_t *>(&h);
@@ -559,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float f = denom > 0.f ? rsc / denom : 0.f;
       const int Hq = P.hkv * G;
       __nv_bfloat16 *orow = P.out + ((q0 + (row_valid ? tr : 0)) * Hq + kvh * G + g) * kD;
-#pragma unroll
+#pragma unroll 1
       for (int cb = 0; cb < kD / 32; ++cb) {
         uint32_t rr[32];
         TC_LD32(tO + cb * 32, rr);
