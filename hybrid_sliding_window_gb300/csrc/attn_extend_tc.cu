@@ -10,7 +10,8 @@
 //   * the CTA owns two 128-row Q tiles, each (128/G) consecutive query tokens
 //     x the G query heads of one KV head, so every K/V tile it loads feeds two
 //     QK^T and two PV products;
-//   * warp 9 gathers the Q rows once (cp.async) and then, from one lane,
+//   * all threads gather the Q rows once (cp.async) while the page rows are
+//     looked up; then warp 9, from one lane,
 //     streams K and V through a two-stage ring with TMA: one 3-D box
 //     {64 dims, 1 head, ps rows} per page and half of D, 128-byte swizzle,
 //     completion counted on "full" mbarriers, slots returned on "empty" ones;
@@ -27,8 +28,9 @@
 //     its output row.
 // KV pools are zero-initialised by the caller (as the pages' pools are), so
 // rows of a loaded page outside the query's key range hold finite values and
-// their zero softmax weight cancels them exactly; the stage buffers are
-// zeroed once at start for the same reason.
+// their zero softmax weight cancels them exactly; page slots of a key tile
+// outside the range load an in-range page of the same request for the same
+// reason.
 // Every mbarrier wait has a poll limit; on expiry the kernel sets an error
 // bit, every role leaves its loop, and the TMEM is still released.
 #include <cuda_bf16.h>
@@ -236,7 +238,7 @@ constexpr int kOffK = 2 * kTileBytes;           // K stage 0, 1
 constexpr int kOffV = 4 * kTileBytes;           // V stage 0, 1
 constexpr int kOffRows = 6 * kTileBytes;        // int32 page rows [max_pages]
 enum { B_FULLK = 0, B_EMPTYK = 2, B_FULLV = 4, B_EMPTYV = 6, B_SDONE = 8, B_PREADY = 10,
-       B_QFULL = 12, B_ODONE = 13, B_COUNT = 14 };
+       B_ODONE = 12, B_COUNT = 13 };
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_extend_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -286,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = (int)((k_hi - kt0) / kKeys + 1);
   const int64_t pg0 = kt0 / P.ps;
   const int n_pg = (int)(k_hi / P.ps - pg0 + 1);
-  if (n_pg > P.max_pages) {
+  if (n_pg > P.max_pages || n_tiles * (kKeys / P.ps) > P.max_pages) {
     if (tid == 0) set_error(P.err, SWA_DEVERR_RANGE);
     return;
   }
@@ -307,16 +309,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_SDONE + i), 1);
       mbar_init(bar(B_PREADY + i), kRows);
     }
-    mbar_init(bar(B_QFULL), 32);
     mbar_init(bar(B_ODONE), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
+  // Q rows of both tiles, gathered by every thread (cp.async, zero fill past
+  // the chunk); their latency overlaps the page-row lookups below.
+  {
+    const int Hq = P.hkv * G;
+    for (int i = tid; i < 2 * kRows * 16; i += kThreads) {
+      const int qt = i / (kRows * 16), rr = (i / 16) % kRows, c = i % 16;
+      const int64_t tok = q0 + qt * T + rr / G;
+      const bool ok = tok < s_qend && (qt * T + rr / G) < n_tok;
+      const __nv_bfloat16 *src = P.q + ((ok ? tok : q0) * Hq + kvh * G + rr % G) * kD + c * 8;
+      cp_async16(sb + kOffQ + qt * kTileBytes + tile_off(rr, c), src, ok);
+    }
+  }
   const int64_t max_page = P.pool_rows / P.ps - 1;
-  for (int i = tid; i < n_pg; i += kThreads) {
+  // Every page slot of every key tile is loaded, so the stage buffers never
+  // hold uninitialised bytes and need no clearing: slots outside the key
+  // range (-1 here) load the item's first in-range page instead, whose
+  // values are finite and get zero weight.  (Not page 0: mapping 0 marks an
+  // evicted SWA slot, which attention must never read.)
+  const int n_slots = n_tiles * (kKeys / P.ps);
+  for (int i = tid; i < n_slots; i += kThreads) {
     const int64_t pos0 = (pg0 + i) * P.ps;
     const int64_t pos = pos0 > k_lo ? pos0 : k_lo;
-    int64_t page = -2;                       // -2: not loaded (outside the key range)
-    if (pos <= k_hi && pos0 + P.ps > k_lo) {
+    int64_t page = -2;                       // -2: outside the key range
+    if (i < n_pg && pos <= k_hi && pos0 + P.ps > k_lo) {
       if (P.kind == SWA_LAYER_FULL) {
         page = P.rt[P.req_idx[b] * P.rt_stride + pos] / P.ps;
       } else {
@@ -333,9 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     s_rows[i] = page == -2 ? -1 : (int32_t)(page * P.page_stride);
   }
-  for (int i = tid; i < 4 * kTileBytes / 16; i += kThreads)
-    reinterpret_cast<uint4 *>(smem + kOffK)[i] = make_uint4(0, 0, 0, 0);
-  fence_async_smem();
+  const int slot_lo = (int)(k_lo / P.ps - pg0);   // first in-range slot
+  asm volatile("cp.async.wait_all;\n" ::: "memory");
+  fence_async_smem();   // Q (written by cp.async) is read by the tensor core
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
@@ -343,18 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kIdO = idesc_f16(128, 128, true);
 
   if (warp == 9) {
-    // ===================== producer: Q gather, then K/V pages =====================
-    const int Hq = P.hkv * G;
-    for (int i = lane; i < 2 * kRows * 16; i += 32) {
-      const int qt = i / (kRows * 16), rr = (i / 16) % kRows, c = i % 16;
-      const int64_t tok = q0 + qt * T + rr / G;
-      const bool ok = tok < s_qend && (qt * T + rr / G) < n_tok;
-      const __nv_bfloat16 *src = P.q + ((ok ? tok : q0) * Hq + kvh * G + rr % G) * kD + c * 8;
-      cp_async16(sb + kOffQ + qt * kTileBytes + tile_off(rr, c), src, ok);
-    }
-    asm volatile("cp.async.wait_all;\n" ::: "memory");
-    fence_async_smem();
-    mbar_arrive(bar(B_QFULL));
+    // ===================== producer: K/V pages =====================
     if (lane == 0) {
       const int pages_per_tile = kKeys / P.ps;
       for (int t = 0; t < n_tiles && !s_abort; ++t) {
@@ -362,20 +370,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kv = 0; kv < 2; ++kv) {
           if (t >= 2 && !mbar_wait(bar((kv ? B_EMPTYV : B_EMPTYK) + s), ((t >> 1) - 1) & 1, &s_abort))
             break;
-          uint32_t bytes = 0;
-          for (int i = 0; i < pages_per_tile; ++i) {
-            const int pi = t * pages_per_tile + i;
-            if (pi < n_pg && s_rows[pi] >= 0) bytes += (uint32_t)P.ps * 256;
-          }
           const uint32_t full = bar((kv ? B_FULLV : B_FULLK) + s);
-          mbar_expect_tx(full, bytes);
+          mbar_expect_tx(full, (uint32_t)kTileBytes);   // every page slot is loaded
           const uint32_t dst = sb + (kv ? kOffV : kOffK) + s * kTileBytes;
           for (int i = 0; i < pages_per_tile; ++i) {
             const int pi = t * pages_per_tile + i;
-            if (pi >= n_pg || s_rows[pi] < 0) continue;
+            const int32_t row = s_rows[pi] >= 0 ? s_rows[pi] : s_rows[slot_lo];
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(dst + h * kHalf + i * P.ps * 128, kv ? &tmV : &tmK, h * 64, kvh,
-                          s_rows[pi], full);
+              tma_load_3d(dst + h * kHalf + i * P.ps * 128, kv ? &tmV : &tmK, h * 64, kvh, row, full);
           }
         }
       }
@@ -403,8 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_ts(tmem + 256 + i * 128, tmem + i * 128 + ks * 8,
                smem_desc(vt + ks * 16 * 128, kHalf, 1024), kIdO, (t > 0 || ks > 0) ? 1u : 0u);
     };
-    if (lane == 0 && mbar_wait(bar(B_QFULL), 0, &s_abort) &&
-        mbar_wait(bar(B_FULLK + 0), 0, &s_abort)) {
+    if (lane == 0 && mbar_wait(bar(B_FULLK + 0), 0, &s_abort)) {
       tc_fence_after();
       issue_s(0, 0);
       issue_s(1, 0);
