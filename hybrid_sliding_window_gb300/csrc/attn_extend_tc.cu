@@ -558,24 +558,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float denom = l_run * rsc + (P.sinks ? exp2f(sg2 - mfin) : 0.f);
       const float f = denom > 0.f ? rsc / denom : 0.f;
       const int Hq = P.hkv * G;
-      __nv_bfloat16 *orow = P.out + ((q0 + (row_valid ? tr : 0)) * Hq + kvh * G + g) * kD;
+      // The warp's 32 output rows go through shared memory (the Q tile area:
+      // every product that read it has completed by ODONE), so that the global
+      // stores are whole 256-byte rows written by 16 consecutive lanes.
+      char *stage = smem + kOffQ + grp * kTileBytes + (warp & 3) * 32 * 256;
 #pragma unroll 1
-      for (int cb = 0; cb < kD / 32; ++cb) {
-        uint32_t rr[32];
-        TC_LD32(tO + cb * 32, rr);
+      for (int cb = 0; cb < kD / 64; ++cb) {
+        uint32_t rr[64];
+        TC_LD32(tO + cb * 64, rr);
+        TC_LD32(tO + cb * 64 + 32, (rr + 32));
         tc_wait_ld();
-        if (row_valid) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint32_t w[4];
+        for (int e = 0; e < 64; e += 8) {
+          uint32_t w[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(rr[e + 2 * k]) * f,
-                                                       __uint_as_float(rr[e + 2 * k + 1]) * f);
-              w[k] = *reinterpret_cast<uint32_t *>(&h);
-            }
-            *reinterpret_cast<uint4 *>(orow + cb * 32 + e) = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int k = 0; k < 4; ++k) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(rr[e + 2 * k]) * f,
+                                                     __uint_as_float(rr[e + 2 * k + 1]) * f);
+            w[k] = *reinterpret_cast<uint32_t *>(&h);
           }
+          const int c = (cb * 64 + e) >> 3;   // 16-byte chunk of the row
+          *reinterpret_cast<uint4 *>(stage + lane * 256 + ((c ^ (lane & 15)) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      __syncwarp();
+#pragma unroll 4
+      for (int idx = lane; idx < 32 * 16; idx += 32) {
+        const int i = idx >> 4, c = idx & 15;
+        const int rw = (warp & 3) * 32 + i;     // row of Q tile grp
+        const int trw = grp * T + rw / G;
+        if (trw < n_tok) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(stage + i * 256 + ((c ^ (i & 15)) << 4));
+          *reinterpret_cast<uint4 *>(P.out + ((q0 + trw) * Hq + kvh * G + rw % G) * kD + c * 8) = v;
         }
       }
     }
