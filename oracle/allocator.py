@@ -306,3 +306,121 @@ def evict_swa(alloc: TwoPoolAllocator, req_to_token, req_idx, pre_lens,
             freed += (alloc.swa.available_size() - before) // alloc.page_size
             out[b] = new
     return out, freed
+
+
+# ---------------------------------------------------------------------------
+# Per-request SWA ring ("SGLang source teardown (15)", section "why sliding
+# windows can be accounted per request": the SWA pool becomes one ring per
+# request slot).
+#
+# The pages give the capacity rule: a ring costs ``ceil(ring_size / ps) * ps``
+# slots and the SWA pool holds one ring per request slot.  They do not print
+# the address of a position inside its ring; the reading taken here is the
+# plain one: request slot ``r`` owns slots ``ps + r * cost .. ps + (r+1) *
+# cost - 1`` (slot range 0..ps-1 stays the padding page, so mapping 0 still
+# means "no SWA slot") and position ``t`` of that request lives at
+# ``ps + r * cost + t % cost``.  Nothing is allocated or released on the SWA
+# side; the mapping is still written (full slot -> ring slot) so translation,
+# the per-batch plan and attention are unchanged, and eviction / free_swa
+# only zero mapping entries.  Reading: a ring must hold the window plus every
+# position stored before the attention that reads it, so a request may add at
+# most ``cost - window_excl`` tokens per call.
+
+def ring_cost(ring_size: int, page_size: int) -> int:
+    """Slots one request's ring occupies: ring_size rounded up to a page."""
+    return ceil_div(int(ring_size), int(page_size)) * int(page_size)
+
+
+def ring_pool_size(req_slots: int, ring_size: int, page_size: int) -> int:
+    """SWA pool capacity in ring mode: one ring per request slot."""
+    return int(req_slots) * ring_cost(ring_size, page_size)
+
+
+def ring_slot(req: int, pos: int, ring_size: int, page_size: int) -> int:
+    """SWA slot of position ``pos`` of the request in slot ``req``."""
+    cost = ring_cost(ring_size, page_size)
+    return int(page_size) + int(req) * cost + int(pos) % cost
+
+
+class _RingSide:
+    """Stands where the SWA page ledger stands in paged mode: nothing to take
+    or give back, the whole pool is always 'available'."""
+
+    def __init__(self, size: int, page_size: int):
+        self.page_size = int(page_size)
+        self.size = int(size)
+        self.num_pages = self.size // self.page_size
+
+    def available_size(self) -> int:
+        return self.size
+
+    def free_slots(self, slots) -> None:
+        pass
+
+    def all_free_pages(self) -> list[int]:
+        return []
+
+
+class RingTwoPoolAllocator(TwoPoolAllocator):
+    """Full pool (paged, as in :class:`TwoPoolAllocator`) + per-request SWA
+    rings.  ``window_excl`` is the largest lookback of the SWA-pool layers;
+    ``ring_size`` must be at least ``window_excl + 1``."""
+
+    def __init__(self, size_full: int, page_size: int, ring_size: int, req_slots: int,
+                 window_excl: int, need_sort: bool = False, init_full=None):
+        if ring_size < window_excl + 1:
+            raise ValueError("ring smaller than the window")
+        self.ring_size = int(ring_size)
+        self.req_slots = int(req_slots)
+        self.window_excl = int(window_excl)
+        self.cost = ring_cost(ring_size, page_size)
+        super().__init__(size_full, ring_pool_size(req_slots, ring_size, page_size), page_size,
+                         need_sort, init_full, None)
+        self.swa = _RingSide(self.size_swa, page_size)
+
+    def available_size(self) -> int:
+        return self.full.available_size()
+
+    def alloc(self, need_size: int):
+        raise ValueError("plain alloc has no request slot in ring mode")
+
+    def alloc_extend(self, prefix_lens, seq_lens, last_loc, req_idx=None, three_part=False):
+        ps = self.page_size
+        pre = [int(x) for x in prefix_lens]
+        seq = [int(x) for x in seq_lens]
+        last = [int(x) for x in last_loc]
+        reqs = [int(x) for x in req_idx]
+        assert len(pre) == len(seq) == len(last) == len(reqs)
+        for p, s, r in zip(pre, seq, reqs):
+            if not 0 <= r < self.req_slots:
+                raise ValueError("request slot outside the rings")
+            if s - p + self.window_excl > self.cost:
+                raise ValueError("more new tokens than the ring holds beside the window")
+        deltas = [ceil_div(s, ps) - ceil_div(p, ps) for p, s in zip(pre, seq)]
+        total = sum(deltas)
+        if not self.full.ensure(total):
+            raise OracleNoMem(total)
+        fp = self.full.take(total)
+        build = extend_slots_three_part if three_part else extend_slots_plain
+        full_out, swa_out = [], []
+        off = 0
+        for r in range(len(pre)):
+            full_out += build(pre[r], seq[r], last[r], fp[off:off + deltas[r]], ps)
+            off += deltas[r]
+            swa_out += [ring_slot(reqs[r], t, self.ring_size, ps) for t in range(pre[r], seq[r])]
+        for f, s in zip(full_out, swa_out):
+            self.mapping[f] = s
+        return full_out, swa_out
+
+    def alloc_decode(self, seq_lens, last_loc, req_idx=None):
+        seq = [int(x) for x in seq_lens]
+        return self.alloc_extend([s - 1 for s in seq], seq, last_loc, req_idx)
+
+    def free_swa(self, full_idx) -> None:
+        for i in full_idx:
+            self.mapping[int(i)] = 0
+
+    def check_no_duplicate_pages(self) -> None:
+        pages = self.full.all_free_pages()
+        assert len(pages) == len(set(pages)), "duplicate free page"
+        assert all(1 <= p <= self.full.num_pages for p in pages)
