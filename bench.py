@@ -175,7 +175,7 @@ def run_native(args, rank, world):
                                            f"layers={args.layers or len(spec.layers)}, "
                                            f"r={args.r or spec.r}, chunk={args.chunk or spec.chunk}]")
     W, K = args.warmup, args.steps
-    st = DecodeState(spec, max_steps=W + 2 * K + 4)
+    st = DecodeState(spec, max_steps=W + 2 * K + 4, swa_ring=args.swa_ring)
     if args.attn_path != -1:
         api.swa_set_attn_path(st.ctx, args.attn_path)
     t0 = time.time()
@@ -270,6 +270,8 @@ def run_native(args, rank, world):
                    "kv_bytes_per_step": int(sum(bytes_steps) / K),
                    "l2": "no flush: each step reads far more KV than the 129 MB L2",
                    "pools_tokens": {"full": st.size_full, "swa": st.size_swa},
+                   "swa_pool": (f"per-request ring of {st.ring_size} tokens" if st.swa_ring
+                                else "paged"),
                    "setup_s": round(setup_s, 1)},
         "hbm_frac": round(value / peak, 4),
         "tokens_per_s": round(spec.batch * world * K / (t_ms_max / 1e3), 1),
@@ -476,6 +478,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="first N layers (profiling only)")
     ap.add_argument("--r", type=float, default=0.0, help="SWA/full token ratio (profiling only)")
     ap.add_argument("--chunk", type=int, default=0, help="prefill chunk (profiling only)")
+    ap.add_argument("--swa-ring", action="store_true",
+                    help="per-request SWA rings instead of the paged SWA pool")
     ap.add_argument("--attn-path", type=int, default=-1,
                     help="-1 best kernels (default); 1 cp.async decode; 0 generic (diagnostics)")
     args = ap.parse_args()

@@ -49,7 +49,8 @@ class swa_config(C.Structure):
                 ("need_sort", C.c_int32), ("max_batch", C.c_int32),
                 ("layers", C.POINTER(swa_layer)),
                 ("full_envelope", C.c_void_p), ("full_envelope_bytes", C.c_int64),
-                ("swa_envelope", C.c_void_p), ("swa_envelope_bytes", C.c_int64)]
+                ("swa_envelope", C.c_void_p), ("swa_envelope_bytes", C.c_int64),
+                ("swa_ring_size", C.c_int32), ("ring_slots", C.c_int32)]
 
 
 class swa_state_view(C.Structure):
@@ -153,9 +154,10 @@ class SwaCtx:
     def __init__(self, layers, page_size, size_full, size_swa, num_q_heads, head_dim,
                  kv_dtype, layout=LAYOUT_PER_LAYER, need_sort=False, max_batch=256,
                  full_envelope=None, swa_envelope=None, init_free_full=None,
-                 init_free_swa=None, device="cuda", stream=None):
+                 init_free_swa=None, device="cuda", stream=None, ring_size=0, ring_slots=0):
         """``layers``: list of dicts with keys kind, window, num_kv_heads and,
-        for the per-layer layout, k / v tensors."""
+        for the per-layer layout, k / v tensors.  ``ring_size`` > 0 selects
+        per-request SWA rings (``size_swa`` = ``ring_slots`` x ring cost)."""
         arr = (swa_layer * len(layers))()
         for i, d in enumerate(layers):
             arr[i].kind = d["kind"]
@@ -179,6 +181,8 @@ class SwaCtx:
         cfg.full_envelope_bytes = full_envelope.numel() if full_envelope is not None else 0
         cfg.swa_envelope = _ptr(swa_envelope)
         cfg.swa_envelope_bytes = swa_envelope.numel() if swa_envelope is not None else 0
+        cfg.swa_ring_size = ring_size
+        cfg.ring_slots = ring_slots
         self.cfg = cfg
         self._layers_arr = arr
         self.layers = layers

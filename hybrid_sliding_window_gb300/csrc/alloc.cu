@@ -143,7 +143,15 @@ __global__ void k_alloc_extend(int bs, const int64_t *pre, const int64_t *seq,
     last_s = mapping[last_f];
   }
   const int64_t open_end = cdiv(p_r, ps) * ps;
-  if (threadIdx.x == 0 && p_r < open_end && (last_f < 0 || last_s <= 0))
+  // Per-request ring: the SWA slot is a function of (request slot, position).
+  const bool ring = swa.ring_cost > 0;
+  int64_t ring_base = -1;
+  if (ring) {
+    const int64_t rq = req_idx[r];
+    if (rq >= 0 && rq < swa.ring_slots) ring_base = ps + rq * swa.ring_cost;
+    else if (threadIdx.x == 0) set_error(err, SWA_DEVERR_RANGE);
+  }
+  if (threadIdx.x == 0 && p_r < open_end && (last_f < 0 || (!ring && last_s <= 0)))
     set_error(err, SWA_DEVERR_RANGE);
   const int64_t first_new = cdiv(p_r, ps);
   const int64_t hf = *full.head, hs = *swa.head;
@@ -156,10 +164,10 @@ __global__ void k_alloc_extend(int bs, const int64_t *pre, const int64_t *seq,
     } else {
       int64_t k = t / ps - first_new;
       int64_t pf = full.ring[ring_pos(hf, page_off + k, full.cap)];
-      int64_t pw = swa.ring[ring_pos(hs, page_off + k, swa.cap)];
       f = pf * ps + t % ps;
-      s = pw * ps + t % ps;
+      s = ring ? 0 : swa.ring[ring_pos(hs, page_off + k, swa.cap)] * ps + t % ps;
     }
+    if (ring) s = ring_base >= 0 ? ring_base + t % swa.ring_cost : 0;
     int64_t o = out_off + (t - p_r);
     out_full[o] = f;
     if (out_swa) out_swa[o] = s;
@@ -185,8 +193,10 @@ __global__ void k_alloc_commit(int bs, const int64_t *pre, const int64_t *seq,
   if (threadIdx.x == 0) {
     *full.head = (*full.head + dp) % full.cap;
     *full.count -= dp;
-    *swa.head = (*swa.head + dp) % swa.cap;
-    *swa.count -= dp;
+    if (swa.ring_cost == 0) {   // per-request rings take no pages
+      *swa.head = (*swa.head + dp) % swa.cap;
+      *swa.count -= dp;
+    }
   }
 }
 
@@ -320,6 +330,15 @@ __global__ void k_release(const int64_t *idx, int64_t n, int do_full, int ps,
     __syncthreads();
     release_bitmap(bm, full, need_sort, expect_full, err);
   }
+  if (swa.ring_cost > 0) {   // per-request rings: nothing to release, only unmap
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+      int64_t f = idx[i];
+      if (f >= 0 && f < map_len - 1) mapping[f] = 0;
+      else set_error(err, SWA_DEVERR_RANGE);
+    }
+    return;
+  }
   const int64_t words = (swa.cap + 1 + 31) / 32;
   for (int64_t w = threadIdx.x; w < words; w += blockDim.x) bm[w] = 0;
   __syncthreads();
@@ -404,6 +423,13 @@ __global__ void k_evict_apply(int bs, const int32_t *rt, int64_t rt_stride,
   if (n == 0) return;
   const int64_t old_p = sc.old_pos[b], new_p = sc.new_pos[b];
   const int64_t row = req_idx[b] * rt_stride;
+  if (swa.ring_cost > 0) {   // per-request rings: the slid-out tokens are only unmapped
+    for (int64_t t = old_p + threadIdx.x; t < new_p; t += blockDim.x) {
+      int64_t f = rt[row + t];
+      if (f > 0 && f < map_len - 1) mapping[f] = 0;
+    }
+    return;
+  }
   int64_t P2 = 1;
   while (P2 < n) P2 <<= 1;
   for (int64_t k = threadIdx.x; k < P2; k += blockDim.x) {
@@ -456,7 +482,7 @@ __global__ void k_evict_commit(int bs, int64_t *evicted, PoolDev swa,
                                EvictScratch sc, int64_t *counters, int need_sort) {
   for (int b = threadIdx.x; b < bs; b += blockDim.x)
     if (sc.npages[b] > 0) evicted[b] = sc.new_pos[b];
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && swa.ring_cost == 0) {
     int64_t total = counters[8];
     if (need_sort) {
       *swa.nstaged += total;

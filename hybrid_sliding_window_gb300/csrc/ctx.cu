@@ -116,8 +116,23 @@ swa_status check_config(const swa_config *cfg, Ctx &c) {
       return fail(nullptr, SWA_ERR_INVALID, "layer " + std::to_string(l) + ": null K/V");
     c.layers.push_back(L);
   }
-  if (c.L_swa > 0 && cfg->size_swa <= (int64_t)c.lookback + ps)
+  if (cfg->swa_ring_size < 0 || cfg->ring_slots < 0)
+    return fail(nullptr, SWA_ERR_CONFIG, "negative swa_ring_size or ring_slots");
+  c.ring_cost = 0;
+  c.ring_slots = 0;
+  if (cfg->swa_ring_size > 0) {
+    // Per-request rings: one ring of ceil(ring / ps) * ps slots per request slot.
+    const int64_t cost = cdiv(cfg->swa_ring_size, ps) * ps;
+    if (cfg->ring_slots < 1) return fail(nullptr, SWA_ERR_CONFIG, "ring mode needs ring_slots >= 1");
+    if (cfg->swa_ring_size < (int64_t)c.lookback + 1)
+      return fail(nullptr, SWA_ERR_CONFIG, "swa_ring_size is smaller than the window");
+    if (cfg->size_swa != (int64_t)cfg->ring_slots * cost)
+      return fail(nullptr, SWA_ERR_CONFIG, "ring mode: size_swa must equal ring_slots * ring cost");
+    c.ring_cost = cost;
+    c.ring_slots = cfg->ring_slots;
+  } else if (c.L_swa > 0 && cfg->size_swa <= (int64_t)c.lookback + ps) {
     return fail(nullptr, SWA_ERR_CONFIG, "SWA pool cannot hold one request (N_swa <= W + P)");
+  }
   // Row addressing.
   for (int l = 0; l < cfg->num_layers; ++l) {
     swa::LayerInfo &L = c.layers[l];
@@ -248,6 +263,8 @@ swa_status swa_ctx_create(const swa_config *cfg, void *state_dev, const int64_t 
                         reinterpret_cast<int64_t *>(base + L.staged_swa),
                         c->counters + SWA_CTR_SWA_HEAD, c->counters + SWA_CTR_SWA_COUNT,
                         c->counters + SWA_CTR_SWA_STAGED, c->np_swa};
+  c->swa.ring_cost = c->ring_cost;
+  c->swa.ring_slots = c->ring_slots;
   c->err_word = reinterpret_cast<int32_t *>(c->counters + SWA_CTR_ERROR);
   for (int l = 0; l < cfg->num_layers; ++l) swa::make_kv_tensor_maps(*c, l);
   c->h_count_full = c->np_full;
@@ -287,10 +304,12 @@ int64_t swa_available_full(const swa_ctx *c) {
 }
 int64_t swa_available_swa(const swa_ctx *c) {
   if (!c || c->mirror_stale) return -1;
+  if (c->ring_cost) return c->cfg.size_swa;   // rings are never exhausted
   return (c->h_count_swa + c->h_staged_swa) * c->cfg.page_size;
 }
 int64_t swa_available_size(const swa_ctx *c) {
   if (!c || c->mirror_stale) return -1;
+  if (c->ring_cost) return swa_available_full(c);   // only the full pool can run out
   return std::min(swa_available_full(c), swa_available_swa(c));
 }
 
@@ -323,6 +342,7 @@ swa_status swa_alloc(swa_ctx *c, int64_t need, int64_t *out_full, int64_t *out_s
                      swa_stream_t stream) {
   if (!c || need < 0 || (need > 0 && !out_full)) return fail(c, SWA_ERR_INVALID, "bad alloc args");
   if (need % c->cfg.page_size) return fail(c, SWA_ERR_INVALID, "need_size is not page aligned");
+  if (c->ring_cost) return fail(c, SWA_ERR_INVALID, "plain alloc has no request slot in ring mode");
   const int64_t n = need / c->cfg.page_size;
   if (n == 0) return SWA_OK;
   cudaStream_t s = (cudaStream_t)stream;
@@ -346,12 +366,15 @@ static swa_status alloc_common(swa_ctx *c, int32_t bs, const int64_t *pre, const
   if (!seq || !seq_h) return fail(c, SWA_ERR_INVALID, "null lengths");
   if (!last_loc && !rt) return fail(c, SWA_ERR_INVALID, "need last_loc or req_to_token");
   if (rt && (!req_idx || rt_stride < 1)) return fail(c, SWA_ERR_INVALID, "req_to_token needs req_idx");
+  if (c->ring_cost && !req_idx) return fail(c, SWA_ERR_INVALID, "ring mode needs req_idx");
   const int64_t ps = c->cfg.page_size;
   int64_t n_new = 0, n_tok = 0;
   for (int b = 0; b < bs; ++b) {
     const int64_t sq = seq_h[b], pr = pre_h ? pre_h[b] : seq_h[b] - 1;
     if (pr < 0 || sq < pr) return fail(c, SWA_ERR_INVALID, "need 0 <= prefix <= seq");
     if (rt && sq > rt_stride) return fail(c, SWA_ERR_INVALID, "seq exceeds req_to_token row");
+    if (c->ring_cost && sq - pr + c->lookback > c->ring_cost)
+      return fail(c, SWA_ERR_INVALID, "more new tokens than the ring holds beside the window");
     n_new += cdiv(sq, ps) - cdiv(pr, ps);
     n_tok += sq - pr;
   }
@@ -359,12 +382,12 @@ static swa_status alloc_common(swa_ctx *c, int32_t bs, const int64_t *pre, const
   if (n_tok == 0) return SWA_OK;   // nothing to allocate
   cudaStream_t s = (cudaStream_t)stream;
   bool okf = ensure_pages(c, true, n_new, s);
-  bool oks = ensure_pages(c, false, n_new, s);
+  bool oks = c->ring_cost ? true : ensure_pages(c, false, n_new, s);
   if (!okf || !oks) return fail(c, SWA_ERR_NOMEM, "not enough free pages");
   CUDA_TRY(c, swa::launch_alloc_extend(*c, bs, pre, seq, last_loc, out_full, out_swa, rt,
                                         rt_stride, req_idx, 0, s));
   c->h_count_full -= n_new;
-  c->h_count_swa -= n_new;
+  if (!c->ring_cost) c->h_count_swa -= n_new;
   return SWA_OK;
 }
 
@@ -405,7 +428,7 @@ swa_status swa_free(swa_ctx *c, const int64_t *full_idx, int64_t n, int64_t n_fu
   CUDA_TRY(c, swa::launch_release(*c, full_idx, n, true, n_full_pages, n_swa_pages,
                                   (cudaStream_t)stream));
   mirror_release(c, true, n_full_pages);
-  mirror_release(c, false, n_swa_pages);
+  if (!c->ring_cost) mirror_release(c, false, n_swa_pages);
   return SWA_OK;
 }
 
@@ -414,7 +437,7 @@ swa_status swa_free_swa(swa_ctx *c, const int64_t *full_idx, int64_t n, int64_t 
   if (!c || n < 0 || (n > 0 && !full_idx)) return fail(c, SWA_ERR_INVALID, "bad free_swa args");
   if (n == 0) return SWA_OK;
   CUDA_TRY(c, swa::launch_release(*c, full_idx, n, false, -1, n_swa_pages, (cudaStream_t)stream));
-  mirror_release(c, false, n_swa_pages);
+  if (!c->ring_cost) mirror_release(c, false, n_swa_pages);
   return SWA_OK;
 }
 
@@ -451,7 +474,7 @@ swa_status swa_evict_swa(swa_ctx *c, int32_t bs, const int32_t *rt, int64_t rt_s
   CUDA_TRY(c, swa::launch_evict(*c, bs, rt, rt_stride, req_idx, pre_lens, evicted,
                                 protected_lens, interval, radix, kEvictMaxPages,
                                 (cudaStream_t)stream));
-  mirror_release(c, false, total);
+  if (!c->ring_cost) mirror_release(c, false, total);
   std::copy(new_ev.begin(), new_ev.end(), evicted_h);
   return SWA_OK;
 }

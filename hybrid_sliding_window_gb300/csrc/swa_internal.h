@@ -23,6 +23,10 @@ struct PoolDev {
   int64_t *count;
   int64_t *nstaged;
   int64_t cap;        // number of pages of the pool (pages 1..cap)
+  // SWA pool in per-request ring mode: slots of one ring (0: paged pool) and
+  // the number of request slots; the ring of slot r starts at ps + r * ring_cost.
+  int64_t ring_cost = 0;
+  int64_t ring_slots = 0;
 };
 
 // Where the rows of one layer live.  Row of slot t:
@@ -73,6 +77,8 @@ struct Ctx {
   std::vector<LayerInfo> layers;
   int L_full = 0, L_swa = 0;
   int lookback = 0;          // largest lookback of SWA-pool layers
+  int64_t ring_cost = 0;     // per-request SWA ring slots (0: paged SWA pool)
+  int32_t ring_slots = 0;
   int esize = 2;             // bytes per stored element
   int64_t np_full = 0, np_swa = 0;
   int64_t mapping_len = 0;

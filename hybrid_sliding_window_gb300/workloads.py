@@ -129,7 +129,9 @@ class DecodeState:
     """A whole decode workload resident on one GPU."""
 
     def __init__(self, spec: Spec, max_steps: int = 64, device: str = "cuda", trace: bool = False,
-                 poison_page0: bool = False):
+                 poison_page0: bool = False, swa_ring: bool = False):
+        """``swa_ring``: per-request SWA rings (one per request slot, holding the
+        window plus one prefill chunk) instead of the paged SWA pool."""
         self.spec = spec
         self.dev = device
         self.seq0 = spec.seq_lens()
@@ -137,6 +139,12 @@ class DecodeState:
         self.max_steps = max_steps
         self.ps = spec.ps
         nf, ns, M = sizing(spec, self.seq0, max_steps + spec.interval)
+        self.swa_ring = swa_ring
+        self.ring_size = 0
+        if swa_ring:
+            self.ring_size = spec.chunk + spec.lookback()
+            cost = -(-self.ring_size // spec.ps) * spec.ps
+            ns = (self.B + 1) * cost          # one ring per req_to_token row
         self.size_full, self.size_swa, self.mem_budget = nf, ns, M
         self.max_ctx = int(self.seq0.max()) + max_steps + 2 * spec.ps
         self.max_seq_len = int(self.seq0.max()) + max_steps
@@ -174,7 +182,8 @@ class DecodeState:
         self.ctx = api.SwaCtx(gl, spec.ps, nf, ns, spec.Hq, spec.D, DTYPES[spec.dtype],
                               api.LAYOUT_PER_LAYER if spec.layout == "per_layer"
                               else api.LAYOUT_ENVELOPE, False, max(self.B, 1),
-                              self.full_env, self.swa_env, device=device)
+                              self.full_env, self.swa_env, device=device,
+                              ring_size=self.ring_size, ring_slots=(self.B + 1) if swa_ring else 0)
         self.rt = torch.zeros((self.B + 1, self.max_ctx), dtype=torch.int32, device=device)
         self.rows = np.arange(1, self.B + 1, dtype=np.int64)
         self.rows_d = torch.tensor(self.rows, device=device)
@@ -238,6 +247,8 @@ class DecodeState:
         per_req = spec.chunk + spec.lookback() + 2 * spec.ps
         rest = spec.lookback() + 2 * spec.ps
         g = max(1, min(self.B, (self.size_swa - self.B * rest) // per_req))
+        if self.swa_ring:
+            g = self.B                         # every request has its own ring
         for g0 in range(0, self.B, g):
             grp = np.arange(g0, min(self.B, g0 + g))
             while (self.lens[grp] < prompt[grp]).any():

@@ -112,7 +112,32 @@ typedef struct swa_config {
   int64_t full_envelope_bytes;
   void *swa_envelope;     /* ENVELOPE: SWA-pool byte buffer                       */
   int64_t swa_envelope_bytes;
+  int32_t swa_ring_size;  /* > 0: per-request SWA rings (below); 0: paged SWA pool */
+  int32_t ring_slots;     /* ring mode: request slots, req_idx in [0, ring_slots)   */
 } swa_config;
+
+/* Per-request SWA ring ([Pools 15], "why sliding windows can be accounted per
+ * request"): instead of a paged SWA pool, every request slot owns one ring of
+ * cost = ceil(swa_ring_size / page_size) * page_size SWA slots, and the SWA
+ * pool holds exactly one ring per slot: size_swa must equal ring_slots * cost
+ * (the pages' capacity rule).  Position t of the request in slot r lives at
+ * SWA slot page_size + r * cost + t % cost (slots 0 .. page_size-1 stay the
+ * padding page; the in-ring address is this library's reading, the pages do
+ * not print it).  Consequences, all checked here:
+ *   - alloc_extend / alloc_decode take SWA slots from the rings (req_idx is
+ *     required) and still write mapping[full] = swa, so translate, the plan,
+ *     the KV store and attention are unchanged; plain swa_alloc has no request
+ *     slot and is SWA_ERR_INVALID;
+ *   - only the full pool can run out (SWA_ERR_NOMEM); swa_available_swa is
+ *     size_swa and swa_available_size is the full pool's;
+ *   - swa_ring_size must be at least the largest SWA-layer lookback + 1, and a
+ *     call may add at most cost - lookback tokens to a request (the ring holds
+ *     the window plus every token stored before the attention that reads it),
+ *     else SWA_ERR_INVALID;
+ *   - swa_evict_swa and swa_free / swa_free_swa release no SWA pages: they
+ *     zero the mapping entries of the tokens that left the window (so the
+ *     device check on window reads keeps its meaning); the SWA page counts
+ *     passed to them are ignored. */
 
 /* Device pointers into the state blob, for inspection by tests. */
 typedef struct swa_state_view {

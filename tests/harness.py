@@ -30,8 +30,11 @@ class Pair:
 
     def __init__(self, layers, Hq, D, dtype, ps, size_full, size_swa, layout="per_layer",
                  need_sort=False, seed=0, perm_free=False, max_batch=64, max_ctx=512,
-                 max_reqs=8, k_scale=1.0, v_scale=1.0, oracle=True):
+                 max_reqs=8, k_scale=1.0, v_scale=1.0, oracle=True, ring_size=0):
         self.layers = layers          # list of (kind, window, hkv)
+        self.ring = ring_size > 0     # per-request SWA rings, one per req_to_token row
+        if self.ring:
+            size_swa = OA.ring_pool_size(max_reqs + 1, ring_size, ps)
         self.Hq, self.D, self.dtype, self.ps = Hq, D, dtype, ps
         self.seed = seed
         self.k_scale, self.v_scale = k_scale, v_scale
@@ -69,11 +72,16 @@ class Pair:
                               api.LAYOUT_PER_LAYER if layout == "per_layer" else api.LAYOUT_ENVELOPE,
                               need_sort, max_batch, full_env, swa_env,
                               torch.tensor(init_f, device=dev) if init_f is not None else None,
-                              torch.tensor(init_s, device=dev) if init_s is not None else None)
+                              torch.tensor(init_s, device=dev) if init_s is not None else None,
+                              ring_size=ring_size, ring_slots=(max_reqs + 1) if self.ring else 0)
         self.rt = torch.zeros((max_reqs + 1, max_ctx), dtype=torch.int32, device=dev)
         self.oracle = oracle
         if oracle:
-            self.oa = OA.TwoPoolAllocator(size_full, size_swa, ps, need_sort, init_f, init_s)
+            if self.ring:
+                self.oa = OA.RingTwoPoolAllocator(size_full, ps, ring_size, max_reqs + 1,
+                                                  self.lookback, need_sort, init_f)
+            else:
+                self.oa = OA.TwoPoolAllocator(size_full, size_swa, ps, need_sort, init_f, init_s)
             self.op = OK.OraclePools(layers, size_full, size_swa, ps, D, dtype, layout)
             self.ort = np.zeros((max_reqs + 1, max_ctx), dtype=np.int64)
         self.sinks = [synth.sinks(seed, l, Hq) for l in range(len(layers))]
@@ -115,7 +123,10 @@ class Pair:
         pos = [t for r, p, s in zip(rows, pre, seq) for t in range(p, s)]
         if self.oracle:
             last = [int(self.ort[r, p - 1]) if p > 0 else -1 for r, p in zip(rows, pre)]
-            of, osw = self.oa.alloc_extend(pre, seq, last)
+            if self.ring:
+                of, osw = self.oa.alloc_extend(pre, seq, last, rows)
+            else:
+                of, osw = self.oa.alloc_extend(pre, seq, last)
             for i, (r, t) in enumerate(zip(reqs, pos)):
                 self.ort[r, t] = of[i]
             if check_alloc:
@@ -220,6 +231,8 @@ class Pair:
         np.testing.assert_array_equal(self.ctx.mapping().cpu().numpy(),
                                       np.array(self.oa.mapping, np.int64))
         for full, led in ((True, self.oa.full), (False, self.oa.swa)):
+            if not full and self.ring:
+                continue          # rings: the SWA free list is never touched
             free, staged = self.ctx.free_list(full)
             assert free == led.free
             assert sorted(staged) == sorted(p for s in led.staged for p in s)
@@ -268,7 +281,10 @@ OKIND = {FULL: OT.FULL, SLIDING: OT.SLIDING, CHUNKED: OT.CHUNKED}
 def replay(st: DecodeState):
     """The oracle allocator driven by the GPU state's recorded calls."""
     spec = st.spec
-    oa = OA.TwoPoolAllocator(st.size_full, st.size_swa, spec.ps)
+    if st.swa_ring:
+        oa = OA.RingTwoPoolAllocator(st.size_full, spec.ps, st.ring_size, st.B + 1, spec.lookback())
+    else:
+        oa = OA.TwoPoolAllocator(st.size_full, st.size_swa, spec.ps)
     ort = np.zeros(tuple(st.rt.shape), np.int64)
     for op in st.trace:
         if op[0] == "evict":
@@ -281,7 +297,10 @@ def replay(st: DecodeState):
                 _, rows, seq = op
                 pre = [s - 1 for s in seq]
             last = [int(ort[r, p - 1]) if p > 0 else -1 for r, p in zip(rows, pre)]
-            full, _ = oa.alloc_extend(pre, seq, last)
+            if st.swa_ring:
+                full, _ = oa.alloc_extend(pre, seq, last, rows)
+            else:
+                full, _ = oa.alloc_extend(pre, seq, last)
             off = 0
             for r, p, s in zip(rows, pre, seq):
                 ort[r, p:s] = full[off:off + s - p]
@@ -294,6 +313,8 @@ def check_state(st, oa, ort):
     assert api.swa_device_check(st.ctx) == 0
     np.testing.assert_array_equal(st.ctx.mapping().cpu().numpy(), np.array(oa.mapping, np.int64))
     for full, led in ((True, oa.full), (False, oa.swa)):
+        if not full and st.swa_ring:
+            continue          # rings: the SWA free list is never touched
         free, _ = st.ctx.free_list(full)
         assert free == led.free
     np.testing.assert_array_equal(st.rt.cpu().numpy().astype(np.int64), ort)

@@ -4,7 +4,8 @@ trace (bit exact), and sampled attention outputs (all query heads of sampled
 requests and layers) against the oracle's brute-force softmax over the
 generator's K/V at the attended positions.
 
-Workloads: MiMo-shaped decode (48 layers, B=64, 4K-32K), GPT-OSS-shaped decode
+Workloads: MiMo-shaped decode (48 layers, B=64, 4K-32K; paged SWA pool and per-request
+SWA rings), GPT-OSS-shaped decode
 (24 layers, B=128, 1K-16K), Llama4-shaped decode (48 layers, FP8 envelope,
 B=16 at 131072), and the MiMo-shaped chunked-prefill extend (B=4, 24576 + 8192)."""
 import gc
@@ -31,9 +32,9 @@ def _free(st):
     torch.cuda.empty_cache()
 
 
-def _decode_case(name, layers, requests, steps=2):
+def _decode_case(name, layers, requests, steps=2, swa_ring=False):
     spec = SPECS[name]
-    st = DecodeState(spec, max_steps=steps + 2, trace=True)
+    st = DecodeState(spec, max_steps=steps + 2, trace=True, swa_ring=swa_ring)
     st.prefill()
     st.alloc_decode_buffers()
     inputs = st.make_decode_inputs(steps)
@@ -57,6 +58,11 @@ def _decode_case(name, layers, requests, steps=2):
 
 def test_mimo_decode_full_size():
     _decode_case("mimo", layers=[0, 4, 44, 47], requests=[7])
+
+
+def test_mimo_decode_full_size_swa_ring():
+    """The same workload with per-request SWA rings instead of the paged SWA pool."""
+    _decode_case("mimo", layers=[0, 4, 44], requests=[7], swa_ring=True)
 
 
 def test_gptoss_decode_full_size():
