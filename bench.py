@@ -175,7 +175,8 @@ def run_native(args, rank, world):
                                            f"layers={args.layers or len(spec.layers)}, "
                                            f"r={args.r or spec.r}, chunk={args.chunk or spec.chunk}]")
     W, K = args.warmup, args.steps
-    st = DecodeState(spec, max_steps=W + 2 * K + 4, swa_ring=args.swa_ring)
+    # Step headroom: the timed steps plus one speculative step's drafts (<= 1024).
+    st = DecodeState(spec, max_steps=W + 2 * K + 4 + 1024, swa_ring=args.swa_ring)
     if args.attn_path != -1:
         api.swa_set_attn_path(st.ctx, args.attn_path)
     t0 = time.time()
@@ -248,6 +249,7 @@ def run_native(args, rank, world):
     barrier()
     e2e_ms = x0.elapsed_time(x1)
     assert api.swa_device_check(st.ctx) == 0
+    spec_alloc = spec_alloc_rate(st) if rank == 0 else None
 
     t_ms_max = t_ms
     e2e_max = e2e_ms
@@ -284,6 +286,7 @@ def run_native(args, rank, world):
         "clocks": clocks,
         "gpu_launches": st.launches_per_step() * K,
         "attn_path": api.swa_last_attn_path(st.ctx),
+        "spec_alloc": spec_alloc,
     }
     if world == 1 and not args.no_extend:
         # The other two figures the metric names: extend TFLOP/s and evict
@@ -404,6 +407,48 @@ def run_extend(args, rank, world, quiet=False):
         "clocks": clocks, "attn_path": api.swa_last_attn_path(st.ctx),
         "gpu_launches": len(spec.layers) * K,
     }
+
+
+def spec_alloc_rate(st):
+    """One speculative decode step's allocation over the whole batch (a draft
+    tree of 4 branches x 3 steps, 8 draft tokens: alloc_len slots per request
+    through swa_alloc_extend), timed with CUDA events; the drafts' new pages
+    are returned afterwards."""
+    import numpy as np
+    import torch
+    from hybrid_sliding_window_gb300 import api
+    ps = st.ps
+    L = api.swa_decode_alloc_sizes(1, 3, 4, 8, True, ps)[0]
+    pre = st.lens.copy()
+    seq = pre + L
+    if int(seq.max()) > st.rt.shape[1]:
+        return None
+    n = int(st.B * L)
+    out_f = torch.empty(n, dtype=torch.int64, device=st.dev)
+    out_s = torch.empty(n, dtype=torch.int64, device=st.dev)
+    d_pre = torch.tensor(pre, device=st.dev)
+    d_seq = torch.tensor(seq, device=st.dev)
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a0.record()
+    api.swa_alloc_extend(st.ctx, d_pre, d_seq, None, pre, seq, out_f, out_s,
+                         req_to_token=st.rt, req_idx=st.rows_d)
+    a1.record()
+    torch.cuda.synchronize()
+    ms = a0.elapsed_time(a1)
+    # Return the drafts' whole new pages (positions from the next page boundary on).
+    keep = -(-pre // ps) * ps
+    idx = torch.cat([st.rt[int(r), int(k):int(s)].to(torch.int64)
+                     for r, k, s in zip(st.rows, keep, seq)])
+    pages = int((-(-(seq - keep) // ps)).sum())
+    if idx.numel():
+        api.swa_free(st.ctx, idx, pages, 0 if st.swa_ring else pages)
+    for r, p in zip(st.rows, pre):
+        st.rt[int(r), int(p):].zero_()
+    assert api.swa_device_check(st.ctx) == 0
+    return {"alloc_len": int(L), "slots": n, "ms": round(ms, 4),
+            "slots_per_s": round(n / (ms / 1e3), 1)}
 
 
 # Sources of the dominant kernel of each bench line: its DRAM traffic, taken

@@ -65,6 +65,7 @@ I32, I64, F32, SZ = C.c_int32, C.c_int64, C.c_float, C.c_size_t
 # name -> (restype, argtypes): mirrors include/swa.h and include/swa_synth.h
 SIGNATURES = {
     "swa_pool_sizes": (I32, [I64, I64, I64, I32, I32, C.c_double, I32, I32, P, P]),
+    "swa_decode_alloc_sizes": (I32, [I32, I32, I32, I32, I32, I32, P, P, P]),
     "swa_state_bytes": (SZ, [P]),
     "swa_ctx_create": (I32, [P, P, P, P, P, P]),
     "swa_ctx_destroy": (None, [P]),
@@ -242,6 +243,17 @@ def swa_pool_sizes(mem_bytes, F, S, L_full, L_swa, r, page_size, window):
                               C.byref(nf), C.byref(ns))
     _check(st, None)
     return nf.value, ns.value
+
+
+def swa_decode_alloc_sizes(algo, steps, topk, draft_tokens, has_draft_kv, page_size):
+    """(alloc_len, reserve, rt_extra) per request per decode step;
+    draft_tokens None means "not given"."""
+    a, r, e = C.c_int64(), C.c_int64(), C.c_int64()
+    st = lib().swa_decode_alloc_sizes(algo, steps, topk, -1 if draft_tokens is None else draft_tokens,
+                                      1 if has_draft_kv else 0, page_size, C.byref(a), C.byref(r),
+                                      C.byref(e))
+    _check(st, None)
+    return a.value, r.value, e.value
 
 
 def swa_available_size(ctx):

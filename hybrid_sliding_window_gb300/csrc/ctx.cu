@@ -217,6 +217,37 @@ swa_status swa_pool_sizes(int64_t mem_bytes, int64_t F, int64_t S, int32_t L_ful
   return SWA_OK;
 }
 
+swa_status swa_decode_alloc_sizes(int32_t algo, int32_t steps, int32_t topk,
+                                  int32_t draft_tokens, int32_t has_draft_kv,
+                                  int32_t page_size, int64_t *alloc_len, int64_t *reserve,
+                                  int64_t *rt_extra) {
+  if (!alloc_len || !reserve || !rt_extra || page_size < 1 || algo < SWA_SPEC_NONE ||
+      algo > SWA_SPEC_UNO)
+    return fail(nullptr, SWA_ERR_INVALID, "bad speculative sizing arguments");
+  const int64_t ps = page_size;
+  const int64_t d = draft_tokens > 0 ? draft_tokens : 0;
+  int64_t len = 1;
+  if (algo == SWA_SPEC_UNO) {
+    if (draft_tokens < 0) return fail(nullptr, SWA_ERR_INVALID, "UNO needs draft_tokens");
+    len = d + 1;
+  } else if (algo == SWA_SPEC_DRAFT) {
+    const int64_t s = steps > 1 ? steps : 1, k = topk > 1 ? topk : 1;
+    if (ps == 1 || k == 1 || !has_draft_kv) {
+      len = std::max(s * k, d);
+    } else {
+      const int64_t pages_per_branch = (ps - 1 + s + ps - 1) / ps;
+      len = std::max(pages_per_branch * ps * k, d);
+    }
+  }
+  *alloc_len = len;
+  *reserve = 2 * len;
+  int64_t extra = 4 + d;
+  if (algo != SWA_SPEC_NONE && (ps > 1 || algo == SWA_SPEC_UNO))
+    extra = std::max(extra, 2 * len + ps - 1);
+  *rt_extra = extra;
+  return SWA_OK;
+}
+
 size_t swa_state_bytes(const swa_config *cfg) {
   if (!cfg || cfg->page_size < 1 || cfg->max_batch < 1) return 0;
   return state_layout(cfg).total;

@@ -286,8 +286,16 @@ class DecodeState:
         self.out_swa = torch.empty(self.B, dtype=torch.int64, device=self.dev)
         self.plan = torch.zeros(api.swa_plan_bytes(self.ctx, self.B, 1), dtype=torch.uint8,
                                 device=self.dev)
-        wsb = max(api.swa_attn_decode_ws_bytes(self.ctx, l, self.B, self.max_seq_len)
-                  for l in range(len(spec.layers)))
+        # Decode steps pass their own longest request, anywhere from the
+        # prompt length up to max_seq_len: size for the largest need over that
+        # range (the split size, hence the split count, depends on it).
+        kinds = {}
+        for l, (kind, _, hkv) in enumerate(spec.layers):
+            kinds.setdefault((kind, hkv), l)
+        lo = max(1, int(self.seq0.max()) - 1)
+        wsb = max(api.swa_attn_decode_ws_bytes(self.ctx, l, self.B, m)
+                  for l in kinds.values()
+                  for m in list(range(lo, self.max_seq_len + 1, 16)) + [self.max_seq_len])
         self.ws = torch.zeros(wsb, dtype=torch.uint8, device=self.dev)
         self.outs = [torch.empty((self.B, spec.Hq, spec.D), dtype=self.in_dtype, device=self.dev)
                      for _ in spec.layers]
@@ -307,12 +315,15 @@ class DecodeState:
         api.swa_alloc_decode(self.ctx, inp["seq_d"], None, inp["seq_h"], self.out_full,
                              self.out_swa, req_to_token=self.rt, req_idx=self.rows_d)
         api.swa_plan(self.ctx, self.rt, self.rows_d, None, inp["seq_d"], self.plan, 1)
+        # The longest request of this step (the workspace is sized for the
+        # largest it can reach); the split size follows it.
+        msl = int(inp["seq_h"].max())
         for l in range(len(spec.layers)):
             api.swa_store_kv(self.ctx, l, inp["k"][l], inp["v"][l], self.out_full, self.out_swa)
             ev = attn_events.get(l) if attn_events else None
             if ev is not None:
                 ev[0].record()
-            api.swa_attn_decode(self.ctx, l, self.rt, self.rows_d, inp["seq_d"], self.max_seq_len,
+            api.swa_attn_decode(self.ctx, l, self.rt, self.rows_d, inp["seq_d"], msl,
                                 self.plan, inp["q"][l], self.sinks_d[l], self.scale, self.outs[l],
                                 self.ws)
             if ev is not None:

@@ -170,6 +170,32 @@ swa_status swa_pool_sizes(int64_t mem_bytes, int64_t F, int64_t S,
                           int32_t page_size, int32_t window,
                           int64_t *n_full, int64_t *n_swa);
 
+/* Per-step decode allocation under speculative decoding ([Pools 15], "how
+ * the sizes are set: from the memory budget to pool sizes").  algo:
+ * SWA_SPEC_NONE (plain decode), SWA_SPEC_DRAFT (a draft tree of `topk`
+ * branches, `steps` deep; has_draft_kv = 0 when drafts write no KV of their
+ * own), SWA_SPEC_UNO (`draft_tokens` draft slots plus one clean root).
+ * Outputs, in slots per request:
+ *   alloc_len: one token without speculation; UNO: draft_tokens + 1; page
+ *     size 1, one branch, or no draft KV: max(steps * topk, draft_tokens);
+ *     otherwise every branch may start anywhere in a page and gets its own
+ *     pages: max(ceil((page_size - 1 + steps) / page_size) * page_size * topk,
+ *     draft_tokens);
+ *   reserve: 2 * alloc_len (double buffer for the scheduler's committed
+ *     length lagging the device);
+ *   rt_extra: req_to_token columns beyond the context length: 4 +
+ *     draft_tokens, raised with speculation on pages of more than one slot
+ *     (or UNO) to reserve + page_size - 1.
+ * A speculative step then takes alloc_len slots per request through
+ * swa_alloc_extend (prefix = current length, seq = prefix + alloc_len).
+ * Pure host function; SWA_ERR_INVALID for a null output, page_size < 1, or
+ * UNO without draft_tokens (draft_tokens < 0 means "not given"). */
+enum swa_spec_algo { SWA_SPEC_NONE = 0, SWA_SPEC_DRAFT = 1, SWA_SPEC_UNO = 2 };
+swa_status swa_decode_alloc_sizes(int32_t algo, int32_t steps, int32_t topk,
+                                  int32_t draft_tokens, int32_t has_draft_kv,
+                                  int32_t page_size, int64_t *alloc_len,
+                                  int64_t *reserve, int64_t *rt_extra);
+
 /* ------------------------------------------------------------- lifecycle --
  * swa_state_bytes: size of the device state blob (mapping, free-page rings,
  * staging lists, counters) for `cfg`; the caller allocates it (any
