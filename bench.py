@@ -409,6 +409,88 @@ def run_extend(args, rank, world, quiet=False):
     }
 
 
+def radix_requests(n_req, seed):
+    """Synthetic prefix-cache traffic: requests = one of 16 shared 2048-token
+    prompts + 1024 own tokens (page 64), drawn up front."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    prompts = rng.integers(1, 32000, size=(16, 2048), dtype=np.int32)
+    return [np.concatenate([prompts[rng.integers(16)],
+                            rng.integers(1, 32000, size=1024, dtype=np.int32)])
+            for _ in range(n_req)]
+
+
+def radix_ops(tree, reqs, evict_every=8):
+    """Each request matches, locks, is 'prefilled' (its own tokens get fresh
+    slots, the first 40 % of them slid out of the window), unlocks and is
+    inserted; every few requests the cache is trimmed by SWA then full
+    eviction.  Returns (ops, tokens)."""
+    import numpy as np
+    slot, ops, toks = 10 ** 6, 0, 0
+    is_oracle = hasattr(tree, "take_releases")
+    for i, t in enumerate(reqs):
+        if is_oracle:
+            t = t.tolist()
+            e, slots, node = tree.match(t)
+        else:
+            e, slots, node = tree.match(t, as_numpy=True)
+        span = tree.lock(node) if e else 0
+        own = np.arange(slot, slot + len(t) - e, dtype=np.int64)
+        slot += len(own)
+        ev = ((e + int(0.4 * (len(t) - e))) // 64) * 64
+        if e:
+            tree.unlock(node, span)
+        if is_oracle:
+            tree.insert(t, list(slots) + own.tolist(), ev)
+        else:
+            tree.insert(t, np.concatenate([slots, own]), ev)
+        ops += 2
+        toks += 2 * len(t)
+        if i % evict_every == evict_every - 1:
+            if is_oracle:
+                tree.evict_swa(4096)
+                tree.evict_full(8192)
+                tree.take_releases()
+            else:
+                tree.evict(4096, swa_only=True)
+                tree.evict(8192)
+                tree.releases()
+            ops += 2
+    return ops, toks
+
+
+def run_radix(args, rank, world):
+    """Host-side SWA radix prefix cache: native tree vs the oracle tree."""
+    from hybrid_sliding_window_gb300 import api
+    from oracle.radix import RadixSWA as OracleRadix
+    n = max(64, 64 * args.steps)
+    warm = radix_requests(16, 1)
+    for _ in range(args.warmup):
+        radix_ops(api.RadixSWA(64, 127), warm)
+    reqs = radix_requests(n, 7)
+    t0 = time.perf_counter()
+    ops, toks = radix_ops(api.RadixSWA(64, 127), reqs)
+    dt = time.perf_counter() - t0
+    n_o = 16
+    t1 = time.perf_counter()
+    ops_o, _ = radix_ops(OracleRadix(64, 127), reqs[:n_o])
+    dto = time.perf_counter() - t1
+    return {
+        "metric": "SWA radix prefix cache ops/s (match + insert + eviction)", "value": round(ops / dt, 1),
+        "unit": "ops/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / max(1, args.steps), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int32 tokens / int64 slots",
+        "data": "synthetic",
+        "config": {"workload": f"{n} requests = one of 16 shared 2048-token prompts + 1024 own "
+                               "tokens, page 64, window 127, SWA then full eviction every 8 "
+                               "requests; host C++ tree in libswa (no device work)",
+                   "tokens_per_s": round(toks / dt, 1)},
+        "cpu_baseline": {"value": round(ops_o / dto, 1), "unit": "ops/s", "cores": 1,
+                         "kind": "oracle", "sample": f"{n_o} requests of the same traffic"},
+        "gpu_launches": 0,
+    }
+
+
 def spec_alloc_rate(st):
     """One speculative decode step's allocation over the whole batch (a draft
     tree of 4 branches x 3 steps, 8 draft tokens: alloc_len slots per request
@@ -514,7 +596,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="mimo", choices=["mimo", "gptoss", "llama4", "extend"])
+    ap.add_argument("--workload", default="mimo",
+                    choices=["mimo", "gptoss", "llama4", "extend", "radix"])
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-extend", action="store_true",
                     help="skip the extend / evict figures added to the decode line")
@@ -540,6 +623,8 @@ def main():
         line = run_reference(args, rank, world)
     elif args.workload == "extend":
         line = run_extend(args, rank, world)
+    elif args.workload == "radix":
+        line = run_radix(args, rank, world) if rank == 0 else None
     else:
         line = run_native(args, rank, world)
     if line is not None:

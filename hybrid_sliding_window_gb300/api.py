@@ -66,6 +66,15 @@ I32, I64, F32, SZ = C.c_int32, C.c_int64, C.c_float, C.c_size_t
 SIGNATURES = {
     "swa_pool_sizes": (I32, [I64, I64, I64, I32, I32, C.c_double, I32, I32, P, P]),
     "swa_decode_alloc_sizes": (I32, [I32, I32, I32, I32, I32, I32, P, P, P]),
+    "swa_radix_create": (I32, [I32, I32, P]),
+    "swa_radix_destroy": (None, [P]),
+    "swa_radix_match": (I32, [P, P, I64, P, P, P]),
+    "swa_radix_insert": (I32, [P, P, I64, P, I64]),
+    "swa_radix_lock": (I32, [P, I64, P]),
+    "swa_radix_unlock": (I32, [P, I64, I64]),
+    "swa_radix_evict": (I32, [P, I32, I64, P]),
+    "swa_radix_releases": (I32, [P, P, P, P, P, P]),
+    "swa_radix_sizes": (I32, [P, P, P, P]),
     "swa_state_bytes": (SZ, [P]),
     "swa_ctx_create": (I32, [P, P, P, P, P, P]),
     "swa_ctx_destroy": (None, [P]),
@@ -254,6 +263,80 @@ def swa_decode_alloc_sizes(algo, steps, topk, draft_tokens, has_draft_kv, page_s
                                       C.byref(e))
     _check(st, None)
     return a.value, r.value, e.value
+
+
+class RadixSWA:
+    """The native SWA radix tree (include/swa.h, "radix prefix cache").
+    Host only; releases come back as numpy arrays (see ``apply_releases``)."""
+
+    def __init__(self, page_size, window):
+        h = C.c_void_p()
+        _check(lib().swa_radix_create(page_size, window, C.byref(h)), None)
+        self.h = h
+        self.ps = page_size
+
+    def __del__(self):
+        h = getattr(self, "h", None)
+        if h is not None and _lib is not None:
+            _lib.swa_radix_destroy(h)
+            self.h = None
+
+    def match(self, tokens, as_numpy=False):
+        import numpy as np
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        out = np.empty(max(len(t), 1), np.int64)
+        e, node = C.c_int64(), C.c_int64()
+        _check(lib().swa_radix_match(self.h, t.ctypes.data, len(t), C.byref(e),
+                                     out.ctypes.data, C.byref(node)), None)
+        slots = out[:e.value]
+        return e.value, (slots if as_numpy else slots.tolist()), node.value
+
+    def insert(self, tokens, slots, swa_evicted):
+        import numpy as np
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        s = np.ascontiguousarray(slots, dtype=np.int64)
+        _check(lib().swa_radix_insert(self.h, t.ctypes.data, min(len(t), len(s)), s.ctypes.data,
+                                      swa_evicted), None)
+
+    def lock(self, node):
+        span = C.c_int64()
+        _check(lib().swa_radix_lock(self.h, node, C.byref(span)), None)
+        return span.value
+
+    def unlock(self, node, span):
+        _check(lib().swa_radix_unlock(self.h, node, span), None)
+
+    def evict(self, n_tokens, swa_only=False):
+        freed = C.c_int64()
+        _check(lib().swa_radix_evict(self.h, 1 if swa_only else 0, n_tokens, C.byref(freed)), None)
+        return freed.value
+
+    def releases(self):
+        """(full slots, how many of them still map SWA slots, SWA-only slots)."""
+        import numpy as np
+        pf, ps_ = C.POINTER(C.c_int64)(), C.POINTER(C.c_int64)()
+        nf, nl, ns = C.c_int64(), C.c_int64(), C.c_int64()
+        _check(lib().swa_radix_releases(self.h, C.byref(pf), C.byref(nf), C.byref(nl),
+                                        C.byref(ps_), C.byref(ns)), None)
+        f = np.ctypeslib.as_array(pf, (nf.value,)).copy() if nf.value else np.zeros(0, np.int64)
+        s = np.ctypeslib.as_array(ps_, (ns.value,)).copy() if ns.value else np.zeros(0, np.int64)
+        return f, nl.value, s
+
+    def sizes(self):
+        a, b, c = C.c_int64(), C.c_int64(), C.c_int64()
+        _check(lib().swa_radix_sizes(self.h, C.byref(a), C.byref(b), C.byref(c)), None)
+        return a.value, b.value, c.value
+
+    def apply_releases(self, ctx, stream=None):
+        """Issue the pending releases on ``ctx``: swa_free for full slots,
+        swa_free_swa for SWA-only ones, with exact page counts."""
+        f, live, s = self.releases()
+        ps = self.ps
+        if len(f):
+            swa_free(ctx, torch.tensor(f, device="cuda"), len(f) // ps, live // ps, stream)
+        if len(s):
+            swa_free_swa(ctx, torch.tensor(s, device="cuda"), len(s) // ps, stream)
+        return f, live, s
 
 
 def swa_available_size(ctx):

@@ -196,6 +196,56 @@ swa_status swa_decode_alloc_sizes(int32_t algo, int32_t steps, int32_t topk,
                                   int32_t page_size, int64_t *alloc_len,
                                   int64_t *reserve, int64_t *rt_extra);
 
+/* ------------------------------------------------- radix prefix cache --
+ * SWA component of the radix prefix cache ([SWA note], "prefix cache:
+ * tombstones and the window hit rule").  A host-side tree over token ids that
+ * holds full slots; a node whose SWA KV was released is a tombstone.
+ *   - window: tokens that must hold live SWA KV before a match end (the SWA
+ *     layers' largest lookback).  A match ends at the last page boundary e
+ *     with min(e, window) live tokens before it (fewer than `window` only
+ *     when the run of live tokens reaches the root);
+ *   - full eviction deletes least recently used unlocked leaves; SWA eviction
+ *     makes the least recently used unlocked live node a tombstone, or deletes
+ *     it if it is a leaf (a leaf is never a tombstone; a tombstone left
+ *     childless is deleted too);
+ *   - a lock full-locks the path to the root and SWA-locks the nodes holding
+ *     the last `window` tokens; it returns that span, which the unlock takes;
+ *   - insert at request end: [0, swa_evicted) goes in as a tombstone prefix
+ *     (only ahead of live tokens); a tombstone the request has SWA KV for is
+ *     revived with the request's slots.
+ * Readings (the page is silent): the tree works in whole pages (a trailing
+ * partial page of a key is ignored: its slots stay the caller's); a match
+ * splits the node it ends inside; every node a match passes, and every node
+ * an insert passes or creates, takes the current time stamp in both LRU
+ * lists; ties go to the older node; the request's slots duplicating cached
+ * tokens are released, unless they are the node's own (a prefix the request
+ * took from the tree).
+ * The tree never touches the device.  Every call appends the slots whose KV
+ * must go back to two lists, read (and cleared) with swa_radix_releases:
+ * `full` slots go to swa_free (n_full / page_size full pages,
+ * n_full_live / page_size of them still mapping SWA pages), `swa` slots to
+ * swa_free_swa (n_swa / page_size SWA pages).  The pointers stay valid until
+ * the next swa_radix_releases.  swa_radix_match writes the matched length e,
+ * the slots of tokens [0, e) (slots_out: capacity n, or NULL) and the node
+ * ending at e (0 = root).  SWA_ERR_INVALID for bad arguments, an unknown
+ * node, an unlock that does not match a lock, or swa_evicted not a multiple
+ * of page_size. */
+typedef struct swa_radix swa_radix;
+swa_status swa_radix_create(int32_t page_size, int32_t window, swa_radix **out);
+void swa_radix_destroy(swa_radix *t);
+swa_status swa_radix_match(swa_radix *t, const int32_t *tokens, int64_t n, int64_t *e,
+                           int64_t *slots_out, int64_t *node);
+swa_status swa_radix_insert(swa_radix *t, const int32_t *tokens, int64_t n,
+                            const int64_t *slots, int64_t swa_evicted);
+swa_status swa_radix_lock(swa_radix *t, int64_t node, int64_t *swa_span);
+swa_status swa_radix_unlock(swa_radix *t, int64_t node, int64_t swa_span);
+/* swa_only = 0: full eviction; 1: SWA eviction.  freed: tokens released. */
+swa_status swa_radix_evict(swa_radix *t, int32_t swa_only, int64_t n_tokens, int64_t *freed);
+swa_status swa_radix_releases(swa_radix *t, const int64_t **full, int64_t *n_full,
+                              int64_t *n_full_live, const int64_t **swa, int64_t *n_swa);
+swa_status swa_radix_sizes(const swa_radix *t, int64_t *cached_tokens, int64_t *live_tokens,
+                           int64_t *nodes);
+
 /* ------------------------------------------------------------- lifecycle --
  * swa_state_bytes: size of the device state blob (mapping, free-page rings,
  * staging lists, counters) for `cfg`; the caller allocates it (any

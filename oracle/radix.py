@@ -31,7 +31,8 @@ Readings where the page is silent (the same in the C++ tree):
   both lists; inserting stamps the nodes it passes or creates;
 * where an inserted request duplicates tokens already cached (live, or
   tombstone with the request evicted there too), the request's slots are
-  released; ties in LRU order go to the older node (creation order).
+  released, unless they are the node's own (the request took its prefix from
+  the tree); ties in LRU order go to the older node (creation order).
 * releases are reported, not performed: ``released_full`` lists full slots
   whose full and SWA KV (if mapped) go back (``free``), ``released_swa`` full
   slots whose SWA KV only goes back (``free_swa``), each with page counts.
@@ -200,7 +201,9 @@ class RadixSWA:
                 # the request has SWA KV from ev on: treat the two parts apart
                 self._split(child, ev - pos)
                 continue
-            if child.tomb and pos >= ev:
+            if child.full == val[pos:pos + c]:
+                pass                                      # the request's prefix came from here
+            elif child.tomb and pos >= ev:
                 self._release(child.full)                 # old slots: no SWA KV left
                 child.full = val[pos:pos + c]             # the node is live again
                 child.tomb = False

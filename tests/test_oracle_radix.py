@@ -47,6 +47,11 @@ def test_scripted_scenario():
     assert R.take_releases() == ([20, 21, 22, 23, 34], [])
     e, slots, _ = R.match([1, 2, 3, 4, 5, 6, 7])
     assert (e, slots) == (7, [30, 31, 32, 33, 24, 25, 26])
+    # A request that took its prefix from the tree hands it back unchanged:
+    # only its own new tokens are added, nothing is released.
+    e, slots, _ = R.match([1, 2, 3, 4, 5, 6])
+    R.insert([1, 2, 3, 4, 5, 6, 8, 8], slots + [50, 51], swa_evicted=0)
+    assert R.take_releases() == ([], [])
     # An inserted request evicted everywhere adds no tombstone leaf.
     R.insert([9, 9, 9], [40, 41, 42], swa_evicted=3)
     assert R.take_releases() == ([40, 41, 42], [])
