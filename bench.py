@@ -250,6 +250,7 @@ def run_native(args, rank, world):
     e2e_ms = x0.elapsed_time(x1)
     assert api.swa_device_check(st.ctx) == 0
     spec_alloc = spec_alloc_rate(st) if rank == 0 else None
+    kernel_ids = translate_rate(st) if rank == 0 else None
 
     t_ms_max = t_ms
     e2e_max = e2e_ms
@@ -287,6 +288,7 @@ def run_native(args, rank, world):
         "gpu_launches": st.launches_per_step() * K,
         "attn_path": api.swa_last_attn_path(st.ctx),
         "spec_alloc": spec_alloc,
+        "translate_for_kernel": kernel_ids,
     }
     if world == 1 and not args.no_extend:
         # The other two figures the metric names: extend TFLOP/s and evict
@@ -489,6 +491,31 @@ def run_radix(args, rank, world):
                          "kind": "oracle", "sample": f"{n_o} requests of the same traffic"},
         "gpu_launches": 0,
     }
+
+
+def translate_rate(st, n=1 << 24):
+    """Kernel-facing id translation through a page table (one entry per page
+    of the full pool, 10 % tombstones) for 16M random virtual ids: ids/s."""
+    import torch
+    from hybrid_sliding_window_gb300 import api
+    g = torch.Generator(device=st.dev).manual_seed(5)
+    pages = st.size_full // st.ps
+    v2p = torch.randperm(pages, device=st.dev, generator=g) + 1
+    v2p[torch.rand(pages, device=st.dev, generator=g) < 0.1] = -1
+    virt = torch.randint(0, pages * st.ps, (n,), device=st.dev, generator=g)
+    out = torch.empty_like(virt)
+    mult = 2 * sum(1 for k, _, _ in st.spec.layers if k == 0)
+    for _ in range(3):
+        api.swa_translate_for_kernel(v2p, virt, st.ps, mult, out)
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record()
+    api.swa_translate_for_kernel(v2p, virt, st.ps, mult, out)
+    a1.record()
+    torch.cuda.synchronize()
+    ms = a0.elapsed_time(a1)
+    return {"ids": n, "ms": round(ms, 4), "ids_per_s": round(n / (ms / 1e3), 1),
+            "bytes_per_id": 24}
 
 
 def spec_alloc_rate(st):

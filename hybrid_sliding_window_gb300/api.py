@@ -66,6 +66,7 @@ I32, I64, F32, SZ = C.c_int32, C.c_int64, C.c_float, C.c_size_t
 SIGNATURES = {
     "swa_pool_sizes": (I32, [I64, I64, I64, I32, I32, C.c_double, I32, I32, P, P]),
     "swa_decode_alloc_sizes": (I32, [I32, I32, I32, I32, I32, I32, P, P, P]),
+    "swa_translate_for_kernel": (I32, [P, P, I64, P, I64, I32, I32, P, P]),
     "swa_radix_create": (I32, [I32, I32, P]),
     "swa_radix_destroy": (None, [P]),
     "swa_radix_match": (I32, [P, P, I64, P, P, P]),
@@ -263,6 +264,17 @@ def swa_decode_alloc_sizes(algo, steps, topk, draft_tokens, has_draft_kv, page_s
                                       C.byref(e))
     _check(st, None)
     return a.value, r.value, e.value
+
+
+def swa_translate_for_kernel(v2p, virt, page_size, multiplier, out=None, ctx=None, stream=None):
+    """Kernel-facing ids of virtual token ids through the page table v2p."""
+    if out is None:
+        out = torch.empty_like(virt)
+    st = lib().swa_translate_for_kernel(ctx.handle if ctx is not None else None, _ptr(v2p),
+                                        v2p.numel(), _ptr(virt), virt.numel(), page_size,
+                                        multiplier, _ptr(out), _stream(stream))
+    _check(st, ctx.handle if ctx is not None else None)
+    return out
 
 
 class RadixSWA:

@@ -493,6 +493,26 @@ __global__ void k_evict_commit(int bs, int64_t *evicted, PoolDev swa,
   }
 }
 
+// ------------------------------------------- translate for the kernels ---
+// Virtual token id -> kernel-facing row id through a virtual-to-physical page
+// table: phys * (ps * multiplier) + t % ps, a tombstone page (-1) clamped to 0.
+__global__ void k_translate_for_kernel(const int64_t *v2p, int64_t n_pages, const int64_t *virt,
+                                       int64_t n, int64_t ps, int64_t stride, int64_t *out,
+                                       int32_t *err) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = virt[i];
+    const int64_t page = t >= 0 ? t / ps : -1;
+    if (page < 0 || page >= n_pages) {
+      if (err) atomicOr(err, SWA_DEVERR_RANGE);
+      out[i] = 0;
+      continue;
+    }
+    const int64_t id = v2p[page] * stride + t % ps;
+    out[i] = id > 0 ? id : 0;
+  }
+}
+
 // ------------------------------------------------------------- translate ---
 __global__ void k_translate(const int64_t *full_loc, int64_t n, const int64_t *mapping,
                             int64_t map_len, int64_t *swa_loc, int32_t *err) {
@@ -587,6 +607,15 @@ cudaError_t launch_evict(Ctx &c, int bs, const int32_t *rt, int64_t rt_stride,
                                        c.mapping, c.mapping_len, c.ev, c.counters,
                                        c.cfg.need_sort, c.err_word);
   k_evict_commit<<<1, 256, 0, s>>>(bs, evicted, c.swa, c.ev, c.counters, c.cfg.need_sort);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_translate_for_kernel(const int64_t *v2p, int64_t n_pages, const int64_t *virt,
+                                       int64_t n, int64_t ps, int64_t multiplier, int64_t *out,
+                                       int32_t *err, int sms, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  k_translate_for_kernel<<<grid_for(n, 256, sms > 0 ? sms : 148), 256, 0, s>>>(
+      v2p, n_pages, virt, n, ps, ps * multiplier, out, err);
   return cudaGetLastError();
 }
 

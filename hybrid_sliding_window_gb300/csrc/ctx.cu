@@ -444,6 +444,18 @@ swa_status swa_alloc_decode(swa_ctx *c, int32_t bs, const int64_t *seq_lens,
                       out_swa, req_to_token, rt_stride, req_idx, stream);
 }
 
+swa_status swa_translate_for_kernel(swa_ctx *c, const int64_t *v2p, int64_t n_pages,
+                                    const int64_t *virt, int64_t n, int32_t page_size,
+                                    int32_t multiplier, int64_t *out, swa_stream_t stream) {
+  if (n < 0 || n_pages < 0 || page_size < 1 || multiplier < 1 ||
+      (n > 0 && (!v2p || !virt || !out)))
+    return fail(c, SWA_ERR_INVALID, "bad translate_for_kernel args");
+  CUDA_TRY(c, swa::launch_translate_for_kernel(v2p, n_pages, virt, n, page_size, multiplier, out,
+                                               c ? c->err_word : nullptr, c ? c->num_sms : 0,
+                                               (cudaStream_t)stream));
+  return SWA_OK;
+}
+
 swa_status swa_translate(swa_ctx *c, const int64_t *full_loc, int64_t n, int64_t *swa_loc,
                          swa_stream_t stream) {
   if (!c || n < 0 || (n > 0 && (!full_loc || !swa_loc))) return fail(c, SWA_ERR_INVALID, "bad translate args");

@@ -117,6 +117,10 @@ cudaError_t launch_evict(Ctx &c, int bs, const int32_t *rt, int64_t rt_stride,
                          int radix, int max_pages_per_req, cudaStream_t s);
 cudaError_t launch_translate(Ctx &c, const int64_t *full_loc, int64_t n,
                              int64_t *swa_loc, cudaStream_t s);
+cudaError_t launch_translate_for_kernel(const int64_t *v2p, int64_t n_pages,
+                                       const int64_t *virt, int64_t n, int64_t ps,
+                                       int64_t multiplier, int64_t *out, int32_t *err,
+                                       int sms, cudaStream_t s);
 
 // ---- store.cu ---------------------------------------------------------------
 cudaError_t launch_store(Ctx &c, int layer, const void *k, const void *v,

@@ -325,6 +325,20 @@ swa_status swa_alloc_decode(swa_ctx *ctx, int32_t bs, const int64_t *seq_lens,
                             int64_t rt_stride, const int64_t *req_idx,
                             swa_stream_t stream);
 
+/* Kernel-facing ids through a virtual-to-physical page table ([PR 34602],
+ * multi_ended_allocator.py, "translate_kv_loc_for_kernel"): for each virtual
+ * token id t, out = v2p[t / page_size] * (page_size * multiplier)
+ * + t % page_size, clamped at 0 so a tombstone page (v2p = -1) reads the
+ * page-0 sink.  multiplier = row blocks of one page (2 x the pool's layers in
+ * the envelope layout; with v2p the identity this is the envelope's
+ * kernel_id).  v2p: n_pages int64 on the device; virt, out: n int64 on the
+ * device.  ctx may be NULL (then out-of-range virtual pages are only set to
+ * 0); with a ctx they also set SWA_DEVERR_RANGE.  The allocation policy of
+ * the unified pool behind v2p is not on the pages and not built here. */
+swa_status swa_translate_for_kernel(swa_ctx *ctx, const int64_t *v2p, int64_t n_pages,
+                                    const int64_t *virt, int64_t n, int32_t page_size,
+                                    int32_t multiplier, int64_t *out, swa_stream_t stream);
+
 /* swa_translate: swa_loc[i] = full_to_swa[full_loc[i]], where full_loc -1
  * reads the trailing sentinel (-1) ([SWA note], "attention backend":
  * translate_loc_from_full_to_swa). */

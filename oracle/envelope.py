@@ -68,3 +68,17 @@ def check_envelope(num_pages_total: int, ps: int, num_layers: int,
     if last_view_end > buffer_bytes:
         raise EnvelopeError("buffer lacks the one-envelope tail pad")
     return n_rows
+
+
+def translate_for_kernel(v2p, virt_tokens, ps: int, multiplier: int):
+    """Kernel-facing ids of virtual token ids through a virtual-to-physical
+    page table ([PR 34602], multi_ended_allocator.py,
+    "translate_kv_loc_for_kernel"): id = phys * (ps * multiplier) + t % ps
+    with phys = v2p[t // ps]; a tombstone page (phys = -1) clamps to 0, the
+    page-0 sink.  ``multiplier`` is the row blocks of a page (2L)."""
+    out = []
+    for t in virt_tokens:
+        t = int(t)
+        phys = int(v2p[t // ps])
+        out.append(max(0, phys * ps * multiplier + t % ps))
+    return out

@@ -122,3 +122,28 @@ def test_hit_rule_brute_force(W):
             m = H.match_end(list(bits), n, W)
             assert H.usable_brute(list(bits), m, W)
             assert all(not H.usable_brute(list(bits), e, W) for e in range(m + 1, n + 1))
+
+
+@pytest.mark.parametrize("ps,L", [(1, 1), (4, 3), (64, 12)])
+def test_translate_for_kernel_identity_is_kernel_id(ps, L):
+    """With the identity page table the translation is the envelope's
+    kernel_id; rows then agree with the independent strided index."""
+    pages = 20
+    v2p = list(range(pages))
+    ts = list(range(pages * ps))
+    ids = E.translate_for_kernel(v2p, ts, ps, 2 * L)
+    assert ids == [E.kernel_id(t, ps, L) for t in ts]
+    for t, i in zip(ts[::7], ids[::7]):
+        for l in range(L):
+            assert l * 2 * ps + i == E.row_of_strided(l, False, t, ps, L)
+
+
+def test_translate_for_kernel_tombstone_and_remap():
+    ps, m = 4, 6
+    v2p = [5, -1, 0, 2]
+    ts = [0, 3, 4, 7, 8, 13, 15]
+    assert E.translate_for_kernel(v2p, ts, ps, m) == [
+        5 * 24 + 0, 5 * 24 + 3,      # page 0 -> physical 5
+        0, 0,                        # page 1 is a tombstone: the page-0 sink
+        0 * 24 + 0,                  # page 2 -> physical 0
+        2 * 24 + 1, 2 * 24 + 3]      # page 3 -> physical 2
