@@ -160,7 +160,8 @@ struct Smem {
   static constexpr int kStages = (FP8 && !KM) ? 6 : 3;
   static constexpr int kQ = 16 * D * 2;
   static constexpr int kStageBytes = 2 * kTile * D * kEsz;
-  static constexpr int kMerge = kWarps * 16 * (D + 4) * 4 + 2 * kWarps * 16 * 4;
+  // warp rows of O (D + 4 floats each), then per-row max, sum and weight
+  static constexpr int kMerge = kWarps * 16 * (D + 4) * 4 + 3 * kWarps * 16 * 4;
   static constexpr int kMain = kQ + kStages * kStageBytes;
   static constexpr int kBig = kMain > kMerge ? kMain : kMerge;
   static constexpr int kTotal = kBig > kMergeScratchBytes ? kBig : kMergeScratchBytes;
@@ -264,10 +265,12 @@ __global__ void __launch_bounds__(NW * 32, (Smem<D, FP8, KM, NW>::kMinBlocks))
     if (r < G) qv[k] = *reinterpret_cast<const uint4 *>(P.q + ((int64_t)b * Hq + kvh * G + r) * D + c * 8);
   }
 
-  // ---- page rows of this split, looked up once (one table read per page) ----
-  // Positions of one page occupy consecutive slots of one pool page, so the
-  // row of key j is rowbase[j / ps - pg0] + j % ps.
+  // ---- pages of this split, looked up once (one table read per page) ----
+  // Positions of one page occupy consecutive slots of one pool page, so key j
+  // sits (j % ps) rows past the first row of page j / ps; the table holds the
+  // byte offset of that first row.
   int64_t *s_rb = reinterpret_cast<int64_t *>(smem + S::kTotal);
+  const int rb = (int)P.addr.row_bytes;
   const int64_t pg0 = k0 / P.ps;
   const int n_pg = (int)((k1 - 1) / P.ps - pg0 + 1);
   const int64_t page_stride = (int64_t)P.ps * (P.addr.blocks ? P.addr.blocks : 1);
@@ -280,42 +283,52 @@ __global__ void __launch_bounds__(NW * 32, (Smem<D, FP8, KM, NW>::kMinBlocks))
       set_error(P.err, SWA_DEVERR_RANGE);
       page = 0;
     }
-    s_rb[i] = page * page_stride;
+    s_rb[i] = page * page_stride * rb;
   }
 
   // ---- tile loader ----
   const char *kbase = P.addr.k + (int64_t)kvh * D * kEsz;
   const char *vbase = P.addr.v + (int64_t)kvh * D * kEsz;
   const int ps_shift = P.ps_shift;
+  // Each thread copies one fixed 16-byte chunk c of rows r0, r0 + kRowStep,
+  // ... of every tile (K and V), so its global and shared addresses change
+  // only by the row; positions are counted from the first row of page pg0.
+  constexpr int kThreads = kWarps * 32;
+  constexpr int kRowStep = kThreads / kRowChunks;
+  constexpr int kPasses = kTile / kRowStep;
+  static_assert(kTile % kRowStep == 0, "whole passes per tile");
+  const int lc = tid % kRowChunks, lr0 = tid / kRowChunks;
+  const char *kb_c = kbase + lc * 16, *vb_c = vbase + lc * 16;
+  const int o0 = (int)(k0 - pg0 * P.ps);
+  const int pmask = ps_shift >= 0 ? (1 << ps_shift) - 1 : 0;
   auto load_tile = [&](int t) {
     char *st = sstage + (t % kStages) * S::kStageBytes;
-    const int64_t kt = k0 + (int64_t)t * kTile;
-    for (int i = tid; i < kTile * kRowChunks; i += blockDim.x) {
-      const int r = i / kRowChunks, c = i % kRowChunks;
-      const int64_t j = kt + r;
-      const bool ok = j < k1;
-      int64_t off = 0;
-      if (ok) {
-        int64_t pg, in;
-        if (ps_shift >= 0) {
-          pg = j >> ps_shift;
-          in = j & ((1 << ps_shift) - 1);
-        } else {
-          pg = j / P.ps;
-          in = j % P.ps;
-        }
-        off = (s_rb[pg - pg0] + in) * P.addr.row_bytes + c * 16;
+    const int x0 = o0 + t * kTile;
+    const int nv = (int)min((int64_t)kTile, k1 - (k0 + (int64_t)t * kTile));
+#pragma unroll
+    for (int k = 0; k < kPasses; ++k) {
+      const int r = lr0 + k * kRowStep;
+      const bool ok = r < nv;
+      const int x = x0 + r;
+      int pi, in;
+      if (ps_shift >= 0) {
+        pi = x >> ps_shift;
+        in = x & pmask;
+      } else {
+        pi = x / P.ps;
+        in = x - pi * P.ps;
       }
+      const int64_t off = ok ? s_rb[pi] + (int64_t)in * rb : 0;
       int dk, dv;
       if constexpr (FP8) {
-        dk = kswz8<D>(r, c);
-        dv = kTile * D + vswz8<D>(r, c);
+        dk = kswz8<D>(r, lc);
+        dv = kTile * D + vswz8<D>(r, lc);
       } else {
-        dk = swz<D>(r, c);
-        dv = kTile * D * 2 + swz<D>(r, c);
+        dk = swz<D>(r, lc);
+        dv = kTile * D * 2 + dk;
       }
-      cp_async16(smem_u32(st + dk), kbase + off, ok);
-      cp_async16(smem_u32(st + dv), vbase + off, ok);
+      cp_async16(smem_u32(st + dk), kb_c + off, ok);
+      cp_async16(smem_u32(st + dv), vb_c + off, ok);
     }
   };
   __syncthreads();  // page rows visible
@@ -389,7 +402,9 @@ __global__ void __launch_bounds__(NW * 32, (Smem<D, FP8, KM, NW>::kMinBlocks))
     cp_commit();
     const char *st = sstage + (t % kStages) * S::kStageBytes;
     const char *tv = st + kTile * D * kEsz;
-    const int64_t kbase_j = k0 + (int64_t)t * kTile + warp * 16;
+    // keys of this tile at or past nvt are outside the split (last tile only)
+    const int nvt = (int)min((int64_t)kTile, k1 - (k0 + (int64_t)t * kTile));
+    const int jw = warp * 16;
     if constexpr (KM) {
       // ---- S^T = K Q^T: rows = this warp's 16 keys, columns = heads ----
       float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
@@ -418,9 +433,11 @@ __global__ void __launch_bounds__(NW * 32, (Smem<D, FP8, KM, NW>::kMinBlocks))
       // sa: (key g, head 2c4), (key g, head 2c4+1), (key g+8, head 2c4), (key g+8, head 2c4+1)
       float v[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        v[e] = (sa[e] + sb[e]) * P.qk_scale_log2;
-        if (kbase_j + g + (e >> 1) * 8 >= k1) v[e] = -INFINITY;
+      for (int e = 0; e < 4; ++e) v[e] = (sa[e] + sb[e]) * P.qk_scale_log2;
+      if (nvt < kTile) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (jw + g + (e >> 1) * 8 >= nvt) v[e] = -INFINITY;
       }
       float r0 = fmaxf(v[0], v[2]), r1 = fmaxf(v[1], v[3]);
 #pragma unroll
@@ -526,11 +543,11 @@ __global__ void __launch_bounds__(NW * 32, (Smem<D, FP8, KM, NW>::kMinBlocks))
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int64_t j = kbase_j + nt * 8 + 2 * c4 + (e & 1);
-          float v = s[nt][e] * P.qk_scale_log2;
-          if (j >= k1) v = -INFINITY;
-          s[nt][e] = v;
+        for (int e = 0; e < 4; ++e) s[nt][e] *= P.qk_scale_log2;
+        if (nvt < kTile) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (jw + nt * 8 + 2 * c4 + (e & 1) >= nvt) s[nt][e] = -INFINITY;
         }
         rmax0 = fmaxf(rmax0, fmaxf(s[nt][0], s[nt][1]));
         rmax1 = fmaxf(rmax1, fmaxf(s[nt][2], s[nt][3]));
@@ -675,19 +692,23 @@ __global__ void __launch_bounds__(NW * 32, (Smem<D, FP8, KM, NW>::kMinBlocks))
   const int pstride = part_stride(G, D);
   const int64_t pair = (int64_t)b * P.hkv + kvh;
   float *part = P.partials + (pair * P.max_splits + split) * pstride;
-  for (int e = tid; e < G * D; e += blockDim.x) {
-    const int gg = e / D, d = e % D;
+  // Row statistics once per head (one thread each): the weight of every
+  // warp's partial row, with the softmax denominator and the sink folded in
+  // when this split is the whole request.
+  float *s_cf = sm_l + kWarps * 16;   // [kWarps][16]
+  if (tid < G) {
+    const int gg = tid;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * 16 + gg]);
     const float Mu = M == -INFINITY ? 0.f : M;
-    float L = 0.f, A = 0.f;
+    float f[kWarps], L = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      const float f = exp2f(sm_m[w * 16 + gg] - Mu);
-      L += sm_l[w * 16 + gg] * f;
-      A += sm_o[(w * 16 + gg) * OS + d] * f;
+      f[w] = exp2f(sm_m[w * 16 + gg] - Mu);
+      L += sm_l[w * 16 + gg] * f[w];
     }
+    float scale = 1.f;
     if (single) {
       float Mf = Mu, extra = 0.f;
       if (P.sinks) {
@@ -696,14 +717,40 @@ __global__ void __launch_bounds__(NW * 32, (Smem<D, FP8, KM, NW>::kMinBlocks))
         extra = exp2f(sg - Mf);
       }
       const float r = exp2f(Mu - Mf);
-      P.out[((int64_t)b * Hq + kvh * G + gg) * D + d] =
-          __float2bfloat16_rn(A * r * P.v_scale / (L * r + extra));
+      scale = r * P.v_scale / (L * r + extra);
     } else {
-      part[gg * D + d] = A;
-      if (d == 0) {
-        part[G * D + 2 * gg] = Mu;
-        part[G * D + 2 * gg + 1] = L;
-      }
+      part[G * D + 2 * gg] = Mu;
+      part[G * D + 2 * gg + 1] = L;
+    }
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s_cf[w * 16 + gg] = f[w] * scale;
+  }
+  __syncthreads();
+  // Eight dims per thread and pass: weighted sum of the warps' rows, then one
+  // 16-byte bf16 store (whole request) or two float4 partial stores.
+  for (int e8 = tid; e8 < G * (D / 8); e8 += kThreads) {
+    const int gg = e8 / (D / 8), d0 = (e8 % (D / 8)) * 8;
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float cf = s_cf[w * 16 + gg];
+      const float4 x = *reinterpret_cast<const float4 *>(sm_o + (w * 16 + gg) * OS + d0);
+      const float4 y = *reinterpret_cast<const float4 *>(sm_o + (w * 16 + gg) * OS + d0 + 4);
+      a[0] += cf * x.x; a[1] += cf * x.y; a[2] += cf * x.z; a[3] += cf * x.w;
+      a[4] += cf * y.x; a[5] += cf * y.y; a[6] += cf * y.z; a[7] += cf * y.w;
+    }
+    if (single) {
+      uint4 packed;
+      packed.x = pack2<false>(a[0], a[1]);
+      packed.y = pack2<false>(a[2], a[3]);
+      packed.z = pack2<false>(a[4], a[5]);
+      packed.w = pack2<false>(a[6], a[7]);
+      *reinterpret_cast<uint4 *>(P.out + ((int64_t)b * Hq + kvh * G + gg) * D + d0) = packed;
+    } else {
+      *reinterpret_cast<float4 *>(part + gg * D + d0) = make_float4(a[0], a[1], a[2], a[3]);
+      *reinterpret_cast<float4 *>(part + gg * D + d0 + 4) = make_float4(a[4], a[5], a[6], a[7]);
     }
   }
   if (single) return;
