@@ -655,12 +655,12 @@ bool tma_decode_supported(const Ctx &c, int layer) {
   return c.cfg.kv_dtype == SWA_DTYPE_E4M3 && D == 128;
 }
 
-// Workspace: [work counters, 256 B][partials][tickets]; every decode kernel
-// family keeps its partials past the first 256 bytes, so the counters survive
-// layers of different shapes sharing one workspace.
+// Workspace: [work counters, 256 B][tickets][partials], the layout every
+// attention family shares (the counters and tickets keep their place for
+// layers of different shapes).
 struct WsLayout {
   int split_keys, max_splits;
-  size_t ticket_off, total;
+  size_t part_off, total;
 };
 
 static WsLayout ws_layout(const Ctx &c, int layer, int64_t nq, int max_seq_len) {
@@ -672,8 +672,8 @@ static WsLayout ws_layout(const Ctx &c, int layer, int64_t nq, int max_seq_len) 
   if (w.split_keys > kMaxSplitKeys) w.split_keys = kMaxSplitKeys;
   w.max_splits = (mk + w.split_keys - 1) / w.split_keys;
   const size_t part = (size_t)nq * L.hkv * w.max_splits * part_stride(G, c.cfg.head_dim) * sizeof(float);
-  w.ticket_off = 256 + (part + 255) / 256 * 256;
-  w.total = w.ticket_off + ((size_t)nq * L.hkv * sizeof(int32_t) + 255) / 256 * 256;
+  w.part_off = ws_partials_off(c, nq);
+  w.total = w.part_off + (part + 255) / 256 * 256;
   return w;
 }
 
@@ -709,8 +709,8 @@ cudaError_t launch_attn_decode_tma(Ctx &c, const AttnArgs &a, cudaStream_t s) {
   P.split_keys = w.split_keys;
   P.max_splits = w.max_splits;
   P.work = static_cast<int32_t *>(a.ws);
-  P.partials = reinterpret_cast<float *>(static_cast<char *>(a.ws) + 256);
-  P.tickets = reinterpret_cast<int32_t *>(static_cast<char *>(a.ws) + w.ticket_off);
+  P.partials = reinterpret_cast<float *>(static_cast<char *>(a.ws) + w.part_off);
+  P.tickets = reinterpret_cast<int32_t *>(static_cast<char *>(a.ws) + 256);
   P.err = c.err_word;
   if (fp8) return launch_t<128, true>(c, L, P, s);
   if (c.cfg.head_dim == 128) return launch_t<128, false>(c, L, P, s);

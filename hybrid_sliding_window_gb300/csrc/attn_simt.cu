@@ -269,7 +269,7 @@ int max_keys(const Ctx &c, int layer, int max_seq_len) {
 
 struct WsLayout {
   size_t partial_bytes;
-  size_t ticket_off;
+  size_t part_off;
   size_t total;
   int max_splits;
 };
@@ -280,8 +280,8 @@ WsLayout ws_layout(const Ctx &c, int layer, int64_t nq, int max_seq_len) {
   const int G = c.cfg.num_q_heads / L.hkv;
   w.max_splits = (max_keys(c, layer, max_seq_len) + kSplit - 1) / kSplit;
   w.partial_bytes = (size_t)nq * L.hkv * w.max_splits * G * (c.cfg.head_dim + 2) * sizeof(float);
-  w.ticket_off = 256 + (w.partial_bytes + 255) / 256 * 256;   // first 256 bytes reserved
-  w.total = w.ticket_off + ((size_t)nq * L.hkv * sizeof(int32_t) + 255) / 256 * 256;
+  w.part_off = ws_partials_off(c, nq);   // [reserved][tickets][partials]
+  w.total = w.part_off + (w.partial_bytes + 255) / 256 * 256;
   return w;
 }
 
@@ -330,8 +330,8 @@ cudaError_t launch_attn_simt(Ctx &c, const AttnArgs &a, cudaStream_t s) {
   P.k_scale = c.cfg.kv_dtype == SWA_DTYPE_E4M3 ? a.k_scale : 1.f;
   P.v_scale = c.cfg.kv_dtype == SWA_DTYPE_E4M3 ? a.v_scale : 1.f;
   P.out = a.out;
-  P.partials = reinterpret_cast<float *>(static_cast<char *>(a.ws) + 256);
-  P.tickets = reinterpret_cast<int32_t *>(static_cast<char *>(a.ws) + w.ticket_off);
+  P.partials = reinterpret_cast<float *>(static_cast<char *>(a.ws) + w.part_off);
+  P.tickets = reinterpret_cast<int32_t *>(static_cast<char *>(a.ws) + 256);
   P.max_splits = w.max_splits;
   P.err = c.err_word;
   dim3 grid(w.max_splits, L.hkv, a.nq);

@@ -96,6 +96,20 @@ struct Ctx {
   int device = 0;
 };
 
+// ---- split workspace of the attention kernels -----------------------------
+// [256 B reserved: work counters][tickets][partials].  The ticket block has
+// one size for every layer and every decode batch of a context (max(nq,
+// max_batch) x the largest KV-head count, int32), so decode calls of any
+// layers can share one workspace: the partials of one layer never cover the
+// tickets of another, which are zero between launches.
+inline size_t ws_tickets_bytes(const Ctx &c, int64_t nq) {
+  int hmax = 1;
+  for (const LayerInfo &L : c.layers) hmax = L.hkv > hmax ? L.hkv : hmax;
+  const int64_t n = nq > c.cfg.max_batch ? nq : c.cfg.max_batch;
+  return ((size_t)n * hmax * sizeof(int32_t) + 255) / 256 * 256;
+}
+inline size_t ws_partials_off(const Ctx &c, int64_t nq) { return 256 + ws_tickets_bytes(c, nq); }
+
 // ---- launchers (alloc.cu) -------------------------------------------------
 cudaError_t launch_init_state(Ctx &c, const int64_t *init_full,
                               const int64_t *init_swa, cudaStream_t s);
@@ -157,6 +171,10 @@ struct AttnArgs {
   void *out;
   void *ws;
   size_t ws_bytes;
+  // Decode only, optional: the batch's new K/V rows ([bs][Hkv][D] bf16),
+  // stored at their slots by the attention launch itself before it reads them.
+  const void *k_new, *v_new;
+  const int64_t *full_loc, *swa_loc;
 };
 
 size_t simt_ws_bytes(const Ctx &c, int layer, int64_t nq, int max_seq_len);

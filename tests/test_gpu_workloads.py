@@ -73,6 +73,20 @@ def test_llama4_shaped_small_envelope_fp8(path, expect):
     run_small(spec, steps=40, path=path, expect_path=expect)
 
 
+@pytest.mark.parametrize("path,expect", PATHS)
+def test_split_layers_of_different_shapes_share_workspace(path, expect):
+    """Windowed layers long enough to be split, after full layers of another
+    shape (more splits, another KV-head count) used the same workspace: the
+    split tickets must keep their place whatever the layer's partials size."""
+    spec = small("mimo", layers=[(SLIDING, 2999, 8), (FULL, 0, 4), (SLIDING, 2999, 8),
+                                 (FULL, 0, 4), (SLIDING, 2999, 8)],
+                 batch=3, seq_kind="uniform", seq_lo=4000, seq_hi=9000, chunk=1024, interval=64)
+    run_small(spec, steps=3, path=path, expect_path=expect)
+    spec = small("llama4", layers=[(CHUNKED, 4096, 8), (FULL, 0, 8), (CHUNKED, 4096, 8)],
+                 batch=3, seq_kind="uniform", seq_lo=5000, seq_hi=9000, chunk=1024, interval=64)
+    run_small(spec, steps=3, path=path, expect_path=expect)
+
+
 def test_decode_edge_cases():
     """Length-1 requests (a single key), requests exactly on page and split
     boundaries, and a sliding window longer than the prefix."""
