@@ -98,6 +98,8 @@ SIGNATURES = {
     "swa_plan": (I32, [P, I32, P, I64, P, P, P, I32, P, SZ, P]),
     "swa_attn_decode_ws_bytes": (SZ, [P, I32, I32, I32]),
     "swa_attn_decode": (I32, [P, I32, I32, P, I64, P, P, I32, P, P, P, F32, F32, F32, P, P, SZ, P]),
+    "swa_store_kv_attn_decode": (I32, [P, I32, I32, P, I64, P, P, I32, P, P, P, P, P, P, P, F32,
+                                        F32, F32, P, P, SZ, P]),
     "swa_attn_decode_noalloc_max_bytes": (SZ, []),
     "swa_attn_decode_noalloc": (I32, [P, I32, I32, P, I64, P, P, I32, P, P, P, F32, F32, F32, P,
                                       P]),
@@ -459,6 +461,21 @@ def swa_attn_decode(ctx, layer, req_to_token, req_idx, seq_lens, max_seq_len, pl
                                  _ptr(seq_lens), max_seq_len, _ptr(plan), _ptr(q), _ptr(sinks),
                                  sm_scale, k_scale, v_scale, _ptr(out), _ptr(ws), ws.numel(),
                                  _stream(stream)), ctx.handle)
+
+
+def swa_store_kv_attn_decode(ctx, layer, req_to_token, req_idx, seq_lens, max_seq_len, plan, q,
+                             k_new, v_new, full_loc, swa_loc, sinks, sm_scale, out, ws,
+                             k_scale=1.0, v_scale=1.0, stream=None):
+    """swa_store_kv of the new tokens, then swa_attn_decode (one launch on the
+    tensor-core decode path)."""
+    bs = seq_lens.numel()
+    stride = req_to_token.shape[1] if req_to_token is not None else 0
+    _check(lib().swa_store_kv_attn_decode(ctx.handle, layer, bs, _ptr(req_to_token), stride,
+                                          _ptr(req_idx), _ptr(seq_lens), max_seq_len, _ptr(plan),
+                                          _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(full_loc),
+                                          _ptr(swa_loc), _ptr(sinks), sm_scale, k_scale, v_scale,
+                                          _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+           ctx.handle)
 
 
 def swa_attn_decode_noalloc_max_bytes():

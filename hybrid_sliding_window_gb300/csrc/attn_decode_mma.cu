@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include "kv_codec.cuh"
 #include "split_merge.cuh"
 #include "swa_internal.h"
 
@@ -52,6 +53,13 @@ struct MmaParams {
   int max_splits;
   int split_keys;         // keys per split (a multiple of the tile)
   int32_t *err;
+  // Optional store of the new tokens ([bs][hkv][D] bf16 rows) before reading:
+  // the slot is full_loc (full layers), else swa_loc, else mapping[full_loc].
+  const char *k_new, *v_new;
+  const int64_t *full_loc, *swa_loc, *mapping;
+  int64_t map_len;
+  int in_full;
+  float st_k_scale, st_v_scale;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -144,6 +152,44 @@ __device__ __forceinline__ int64_t key_slot(const MmaParams &P, const ReqRef &R,
   const int64_t page = P.plan.pages[(int64_t)b * P.plan.max_pages + k];
   if (page <= 0) set_error(P.err, SWA_DEVERR_WINDOW_EVICTED);
   return page * P.ps + j % P.ps;
+}
+
+// The new token's row of KV head kvh for request b, written to the pool by
+// the CTA whose key range ends at that token (the only one that reads it);
+// the same bytes as the KV store kernel writes.
+template <int D, bool FP8>
+__device__ __forceinline__ void store_new_token(const MmaParams &P, int b, int kvh, int tid,
+                                                int nthreads) {
+  constexpr int kEsz = FP8 ? 1 : 2;
+  constexpr int kChunks = D * kEsz / 16;   // 16-byte pool chunks of one head row
+  int64_t slot;
+  if (P.in_full) {
+    slot = P.full_loc[b];
+  } else if (P.swa_loc) {
+    slot = P.swa_loc[b];
+  } else {
+    int64_t f = P.full_loc[b];
+    if (f < 0) f += P.map_len;
+    slot = (f >= 0 && f < P.map_len) ? P.mapping[f] : -1;
+  }
+  if (slot < 0 || slot >= P.pool_rows) {
+    if (tid == 0) set_error(P.err, SWA_DEVERR_RANGE);
+    return;
+  }
+  const int64_t row = kv_row(P.addr, slot) * P.addr.row_bytes + (int64_t)kvh * D * kEsz;
+  const int64_t src_row = ((int64_t)b * P.hkv + kvh) * D * 2;   // bf16 input
+  for (int i = tid; i < 2 * kChunks; i += nthreads) {
+    const bool is_v = i >= kChunks;
+    const int c = is_v ? i - kChunks : i;
+    char *dst = (is_v ? P.addr.v : P.addr.k) + row + c * 16;
+    const char *src = (is_v ? P.v_new : P.k_new) + src_row;
+    if constexpr (FP8) {
+      const uint4 *w = reinterpret_cast<const uint4 *>(src + c * 32);
+      *reinterpret_cast<uint4 *>(dst) = e4m3_encode16(w[0], w[1], is_v ? P.st_v_scale : P.st_k_scale);
+    } else {
+      *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src + c * 16);
+    }
+  }
 }
 
 // Shared-memory plan (bytes):
@@ -331,7 +377,10 @@ __global__ void __launch_bounds__(NW * 32, (Smem<D, FP8, KM, NW>::kMinBlocks))
       cp_async16(smem_u32(st + dv), vb_c + off, ok);
     }
   };
-  __syncthreads();  // page rows visible
+  // The new token (fused store): written before the barrier below, so the
+  // tile loads issued after it read the stored row.
+  if (P.k_new != nullptr && k1 == p + 1) store_new_token<D, FP8>(P, b, kvh, tid, kThreads);
+  __syncthreads();  // page rows (and the new token's row) visible
 #pragma unroll
   for (int t = 0; t < kStages - 1; ++t) {
     if (t < n_tiles) load_tile(t);
@@ -779,7 +828,7 @@ int max_keys_of(const Ctx &c, int layer, int max_seq_len) {
 }
 
 struct Layout {
-  size_t ticket_off, total;
+  size_t part_off, total;
   int max_splits, split_keys;
 };
 
@@ -791,8 +840,8 @@ Layout layout_of(const Ctx &c, int layer, int64_t nq, int max_seq_len) {
   w.split_keys = decode_split_keys(c.num_sms, nq, L.hkv, mk, c.cfg.page_size);
   w.max_splits = (mk + w.split_keys - 1) / w.split_keys;
   size_t part = (size_t)nq * L.hkv * w.max_splits * part_stride(G, c.cfg.head_dim) * sizeof(float);
-  w.ticket_off = 256 + (part + 255) / 256 * 256;   // first 256 bytes: reserved counters
-  w.total = w.ticket_off + ((size_t)nq * L.hkv * sizeof(int32_t) + 255) / 256 * 256;
+  w.part_off = ws_partials_off(c, nq);
+  w.total = w.part_off + (part + 255) / 256 * 256;
   return w;
 }
 
@@ -844,11 +893,20 @@ cudaError_t launch_attn_decode_mma(Ctx &c, const AttnArgs &a, cudaStream_t s) {
   P.qk_scale_log2 = a.scale * 1.4426950408889634f * (fp8 ? a.k_scale : 1.f);
   P.v_scale = fp8 ? a.v_scale : 1.f;
   P.out = static_cast<__nv_bfloat16 *>(a.out);
-  P.partials = reinterpret_cast<float *>(static_cast<char *>(a.ws) + 256);
-  P.tickets = reinterpret_cast<int32_t *>(static_cast<char *>(a.ws) + w.ticket_off);
+  P.partials = reinterpret_cast<float *>(static_cast<char *>(a.ws) + w.part_off);
+  P.tickets = reinterpret_cast<int32_t *>(static_cast<char *>(a.ws) + 256);
   P.max_splits = w.max_splits;
   P.split_keys = w.split_keys;
   P.err = c.err_word;
+  P.k_new = static_cast<const char *>(a.k_new);
+  P.v_new = static_cast<const char *>(a.v_new);
+  P.full_loc = a.full_loc;
+  P.swa_loc = a.swa_loc;
+  P.mapping = c.mapping;
+  P.map_len = c.mapping_len;
+  P.in_full = L.in_full ? 1 : 0;
+  P.st_k_scale = a.k_scale;
+  P.st_v_scale = a.v_scale;
   if (w.max_splits > 65535) return cudaErrorInvalidConfiguration;   // grid z limit
   dim3 grid(L.hkv, a.nq, w.max_splits);
   const int D = c.cfg.head_dim;

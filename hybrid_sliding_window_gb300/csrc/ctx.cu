@@ -575,11 +575,17 @@ size_t swa_attn_decode_ws_bytes(const swa_ctx *c, int32_t layer, int32_t bs, int
   return swa::simt_ws_bytes(*c, layer, bs, max_seq_len);
 }
 
-swa_status swa_attn_decode(swa_ctx *c, int32_t layer, int32_t bs, const int32_t *rt,
-                           int64_t rt_stride, const int64_t *req_idx, const int64_t *seq_lens,
-                           int32_t max_seq_len, const void *plan, const void *q,
-                           const float *sinks, float sm_scale, float k_scale, float v_scale,
-                           void *out, void *ws, size_t ws_bytes, swa_stream_t stream) {
+// Decode attention, optionally preceded by the store of the batch's new
+// tokens: on the tensor-core path the attention launch stores them itself,
+// elsewhere the store kernel runs first.
+static swa_status attn_decode_impl(swa_ctx *c, int32_t layer, int32_t bs, const int32_t *rt,
+                                   int64_t rt_stride, const int64_t *req_idx,
+                                   const int64_t *seq_lens, int32_t max_seq_len, const void *plan,
+                                   const void *q, const void *k_new, const void *v_new,
+                                   const int64_t *full_loc, const int64_t *swa_loc,
+                                   const float *sinks, float sm_scale, float k_scale,
+                                   float v_scale, void *out, void *ws, size_t ws_bytes,
+                                   swa_stream_t stream) {
   if (!c) return SWA_ERR_INVALID;
   if (layer < 0 || layer >= c->cfg.num_layers) return fail(c, SWA_ERR_INVALID, "layer out of range");
   if (bs < 0 || bs > c->cfg.max_batch) return fail(c, SWA_ERR_INVALID, "bs out of range");
@@ -588,6 +594,10 @@ swa_status swa_attn_decode(swa_ctx *c, int32_t layer, int32_t bs, const int32_t 
   if (!seq_lens || !q || !out || max_seq_len < 1 || (L.in_full && (!rt || !req_idx)) ||
       (!L.in_full && !plan))
     return fail(c, SWA_ERR_INVALID, "bad attention args");
+  const bool store = k_new || v_new;
+  if (store && (!k_new || !v_new || !full_loc)) return fail(c, SWA_ERR_INVALID, "bad store args");
+  if (store && c->cfg.kv_dtype == SWA_DTYPE_E4M3 && (!(k_scale > 0) || !(v_scale > 0)))
+    return fail(c, SWA_ERR_INVALID, "fp8 scales must be > 0");
   if (bs > 65535) return fail(c, SWA_ERR_INVALID, "bs > 65535");
   if (ws_bytes < swa_attn_decode_ws_bytes(c, layer, bs, max_seq_len) || !ws)
     return fail(c, SWA_ERR_INVALID, "split workspace too small");
@@ -611,10 +621,19 @@ swa_status swa_attn_decode(swa_ctx *c, int32_t layer, int32_t bs, const int32_t 
   a.ws = ws;
   a.ws_bytes = ws_bytes;
   cudaStream_t s = (cudaStream_t)stream;
+  const bool mma = !use_tma(c, layer) && use_mma(c, layer);
+  if (store && mma) {
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.full_loc = full_loc;
+    a.swa_loc = swa_loc;
+  } else if (store) {
+    CUDA_TRY(c, swa::launch_store(*c, layer, k_new, v_new, bs, full_loc, swa_loc, k_scale, v_scale, s));
+  }
   if (use_tma(c, layer)) {
     c->last_path = 3;
     CUDA_TRY(c, swa::launch_attn_decode_tma(*c, a, s));
-  } else if (use_mma(c, layer)) {
+  } else if (mma) {
     c->last_path = 1;
     CUDA_TRY(c, swa::launch_attn_decode_mma(*c, a, s));
   } else {
@@ -622,6 +641,30 @@ swa_status swa_attn_decode(swa_ctx *c, int32_t layer, int32_t bs, const int32_t 
     CUDA_TRY(c, swa::launch_attn_simt(*c, a, s));
   }
   return SWA_OK;
+}
+
+swa_status swa_attn_decode(swa_ctx *c, int32_t layer, int32_t bs, const int32_t *rt,
+                           int64_t rt_stride, const int64_t *req_idx, const int64_t *seq_lens,
+                           int32_t max_seq_len, const void *plan, const void *q,
+                           const float *sinks, float sm_scale, float k_scale, float v_scale,
+                           void *out, void *ws, size_t ws_bytes, swa_stream_t stream) {
+  return attn_decode_impl(c, layer, bs, rt, rt_stride, req_idx, seq_lens, max_seq_len, plan, q,
+                          nullptr, nullptr, nullptr, nullptr, sinks, sm_scale, k_scale, v_scale,
+                          out, ws, ws_bytes, stream);
+}
+
+swa_status swa_store_kv_attn_decode(swa_ctx *c, int32_t layer, int32_t bs, const int32_t *rt,
+                                    int64_t rt_stride, const int64_t *req_idx,
+                                    const int64_t *seq_lens, int32_t max_seq_len, const void *plan,
+                                    const void *q, const void *k_new, const void *v_new,
+                                    const int64_t *full_loc, const int64_t *swa_loc,
+                                    const float *sinks, float sm_scale, float k_scale,
+                                    float v_scale, void *out, void *ws, size_t ws_bytes,
+                                    swa_stream_t stream) {
+  if (c && bs > 0 && (!k_new || !v_new || !full_loc)) return fail(c, SWA_ERR_INVALID, "bad store args");
+  return attn_decode_impl(c, layer, bs, rt, rt_stride, req_idx, seq_lens, max_seq_len, plan, q,
+                          k_new, v_new, full_loc, swa_loc, sinks, sm_scale, k_scale, v_scale, out,
+                          ws, ws_bytes, stream);
 }
 
 size_t swa_attn_extend_ws_bytes(const swa_ctx *c, int32_t layer, int64_t n_tokens,

@@ -15,6 +15,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include "kv_codec.cuh"
 #include "swa_internal.h"
 
 namespace swa {
@@ -36,12 +37,6 @@ struct StoreParams {
   float k_scale, v_scale;
   int32_t *err;
 };
-
-__device__ inline uint32_t pack_e4m3x4(float a, float b, float c, float d) {
-  __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-  __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
-  return (uint32_t)lo | ((uint32_t)hi << 16);
-}
 
 __global__ void k_store(StoreParams P) {
   const int64_t total = P.n * P.chunks_per_row * 2;
@@ -71,22 +66,7 @@ __global__ void k_store(StoreParams P) {
     if (P.dtype == SWA_DTYPE_E4M3) {
       // 16 output bytes <- 16 bf16 inputs (32 bytes).
       const uint4 *src = reinterpret_cast<const uint4 *>(srcrow + (i * P.chunks_per_row + c) * 32);
-      uint4 a = src[0], b = src[1];
-      const float sc = is_v ? P.v_scale : P.k_scale;
-      const __nv_bfloat16 *ha = reinterpret_cast<const __nv_bfloat16 *>(&a);
-      const __nv_bfloat16 *hb = reinterpret_cast<const __nv_bfloat16 *>(&b);
-      float f[16];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        f[e] = __fdiv_rn(__bfloat162float(ha[e]), sc);
-        f[8 + e] = __fdiv_rn(__bfloat162float(hb[e]), sc);
-      }
-      uint4 o;
-      o.x = pack_e4m3x4(f[0], f[1], f[2], f[3]);
-      o.y = pack_e4m3x4(f[4], f[5], f[6], f[7]);
-      o.z = pack_e4m3x4(f[8], f[9], f[10], f[11]);
-      o.w = pack_e4m3x4(f[12], f[13], f[14], f[15]);
-      *reinterpret_cast<uint4 *>(dst) = o;
+      *reinterpret_cast<uint4 *>(dst) = e4m3_encode16(src[0], src[1], is_v ? P.v_scale : P.k_scale);
     } else {
       const uint4 *src = reinterpret_cast<const uint4 *>(srcrow + (i * P.chunks_per_row + c) * 16);
       *reinterpret_cast<uint4 *>(dst) = *src;

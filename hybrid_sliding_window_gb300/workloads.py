@@ -300,10 +300,11 @@ class DecodeState:
         self.outs = [torch.empty((self.B, spec.Hq, spec.D), dtype=self.in_dtype, device=self.dev)
                      for _ in spec.layers]
 
-    def decode_step(self, inp, attn_events=None):
+    def decode_step(self, inp, attn_events=None, fused=True):
         """One decode step: evict (interval), alloc_decode, plan, then per layer
-        store_kv + attn_decode.  attn_events: optional dict layer -> (start,
-        end) CUDA events recorded around that layer's attention launch."""
+        store_kv + attn_decode - one swa_store_kv_attn_decode call when
+        `fused`, else the two calls.  attn_events: optional dict layer ->
+        (start, end) CUDA events recorded around that layer's attention."""
         spec = self.spec
         if self.trace is not None:
             self.trace.append(("evict", self.rows.tolist(), inp["pre_h"].tolist(),
@@ -319,13 +320,21 @@ class DecodeState:
         # largest it can reach); the split size follows it.
         msl = int(inp["seq_h"].max())
         for l in range(len(spec.layers)):
-            api.swa_store_kv(self.ctx, l, inp["k"][l], inp["v"][l], self.out_full, self.out_swa)
+            if not fused:
+                api.swa_store_kv(self.ctx, l, inp["k"][l], inp["v"][l], self.out_full,
+                                 self.out_swa)
             ev = attn_events.get(l) if attn_events else None
             if ev is not None:
                 ev[0].record()
-            api.swa_attn_decode(self.ctx, l, self.rt, self.rows_d, inp["seq_d"], msl,
-                                self.plan, inp["q"][l], self.sinks_d[l], self.scale, self.outs[l],
-                                self.ws)
+            if fused:
+                api.swa_store_kv_attn_decode(self.ctx, l, self.rt, self.rows_d, inp["seq_d"], msl,
+                                             self.plan, inp["q"][l], inp["k"][l], inp["v"][l],
+                                             self.out_full, self.out_swa, self.sinks_d[l],
+                                             self.scale, self.outs[l], self.ws)
+            else:
+                api.swa_attn_decode(self.ctx, l, self.rt, self.rows_d, inp["seq_d"], msl,
+                                    self.plan, inp["q"][l], self.sinks_d[l], self.scale,
+                                    self.outs[l], self.ws)
             if ev is not None:
                 ev[1].record()
         self.lens = inp["seq_h"].copy()

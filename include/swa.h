@@ -425,7 +425,11 @@ swa_status swa_plan(swa_ctx *ctx, int32_t bs, const int32_t *req_to_token,
  * req_to_token, keys of SWA-pool layers through `plan` (built for the same
  * batch).  Long key ranges are split across CTAs and merged in the same
  * launch; `ws` is the split workspace (size from *_ws_bytes) and must be
- * zero-filled before its first use (the kernels leave it reusable).
+ * zero-filled before its first use (the kernels leave it reusable).  Its
+ * layout is [256 B counters][tickets][partials] with a ticket block of one
+ * size per context for batches up to max_batch, so decode calls of any
+ * layers may share one workspace sized for the largest of them; a generic-
+ * path extend call with more query tokens than max_batch needs its own.
  *
  * swa_attn_decode: one query per request at p = seq_lens[b] - 1 (its KV
  * already stored). max_seq_len bounds seq_lens (host; sizes the grid). */
@@ -438,6 +442,34 @@ swa_status swa_attn_decode(swa_ctx *ctx, int32_t layer, int32_t bs,
                            const float *sinks, float sm_scale, float k_scale,
                            float v_scale, void *out, void *ws, size_t ws_bytes,
                            swa_stream_t stream);
+
+/* swa_store_kv_attn_decode: swa_store_kv of the batch's new tokens followed
+ * by swa_attn_decode on the same layer, as one call ([Pools 15], "who writes
+ * into the pages": the decode step stores each layer's new K/V, then that
+ * layer attends over it).  k_new, v_new: [bs][Hkv][D] rows, laid out and
+ * typed as for swa_store_kv (bf16 for bf16 and E4M3 pools, f32 for an F32
+ * pool); row b is request b's token at p = seq_lens[b] - 1, stored at
+ * full_loc[b] (full layers) or swa_loc[b] (SWA-pool layers; NULL =
+ * mapping[full_loc[b]]) - the slots swa_alloc_decode returned, which
+ * req_to_token / plan must map p to.  k_scale / v_scale serve both the E4M3
+ * encoding of the store and the decoding in attention.  Where the
+ * tensor-core decode kernel runs, one launch does both: the CTA whose key
+ * range ends at p writes that token's row of its KV head, then loads it with
+ * its other keys; on the other attention paths the store kernel runs first.
+ * Pools and outputs are identical to the two calls in sequence.  Errors: as
+ * the two calls (an out-of-range slot sets SWA_DEVERR_RANGE and is not
+ * written). */
+swa_status swa_store_kv_attn_decode(swa_ctx *ctx, int32_t layer, int32_t bs,
+                                    const int32_t *req_to_token,
+                                    int64_t rt_stride, const int64_t *req_idx,
+                                    const int64_t *seq_lens,
+                                    int32_t max_seq_len, const void *plan,
+                                    const void *q, const void *k_new,
+                                    const void *v_new, const int64_t *full_loc,
+                                    const int64_t *swa_loc, const float *sinks,
+                                    float sm_scale, float k_scale,
+                                    float v_scale, void *out, void *ws,
+                                    size_t ws_bytes, swa_stream_t stream);
 
 /* swa_attn_decode_noalloc: swa_attn_decode for callers that cannot allocate
  * device memory - engines that give all of HBM to their KV pools at start-up
