@@ -287,7 +287,17 @@ __global__ void __launch_bounds__(NW * 32, (Smem<D, FP8, KM, NW>::kMinBlocks))
   const int G = P.G;
   const int Hq = P.hkv * G;
 
+  // Launched as a programmatic dependent of the previous kernel on the
+  // stream: wait for it (and its memory) before the first global access.
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const ReqRef R = req_ref(P, b);
+  // Windowed layers whose plan row fits one warp: the row's page entries are
+  // read now, with the sequence length and the plan header, instead of after
+  // them (one dependent DRAM round trip fewer before the first tile).
+  const bool pfast = P.kind != SWA_LAYER_FULL && P.plan.max_pages <= 32;
+  int32_t pv = 0;
+  if (pfast && warp == 0 && lane < P.plan.max_pages)
+    pv = P.plan.pages[(int64_t)b * P.plan.max_pages + lane];
   const int64_t p = P.seq[b] - 1;
   int64_t lo = 0;
   if (P.kind == SWA_LAYER_SLIDING) lo = p - P.window > 0 ? p - P.window : 0;
@@ -321,7 +331,31 @@ __global__ void __launch_bounds__(NW * 32, (Smem<D, FP8, KM, NW>::kMinBlocks))
   const int n_pg = (int)((k1 - 1) / P.ps - pg0 + 1);
   const int64_t page_stride = (int64_t)P.ps * (P.addr.blocks ? P.addr.blocks : 1);
   const int64_t max_page = (P.pool_rows / P.ps) - 1;
-  for (int i = tid; i < n_pg; i += blockDim.x) {
+  if (pfast) {
+    // n_pg <= plan pages <= 32: warp 0, lane i takes page pg0 + i from the
+    // lane that read its plan entry (the same checks as key_slot).
+    if (warp == 0) {
+      const int64_t pos = (pg0 + lane) * P.ps > k0 ? (pg0 + lane) * P.ps : k0;
+      const int64_t k = pos / P.ps - R.h2;
+      const int32_t pgv = __shfl_sync(0xffffffffu, pv, (int)(k < 0 ? 0 : (k > 31 ? 31 : k)));
+      if (lane < n_pg) {
+        int64_t slot = 0;
+        if (pos < R.h0 || k < 0 || k >= R.h3) {
+          set_error(P.err, SWA_DEVERR_RANGE);
+        } else {
+          if (pgv <= 0) set_error(P.err, SWA_DEVERR_WINDOW_EVICTED);
+          slot = (int64_t)pgv * P.ps + pos % P.ps;
+        }
+        int64_t page = slot / P.ps;
+        if (slot < 0 || page > max_page) {
+          set_error(P.err, SWA_DEVERR_RANGE);
+          page = 0;
+        }
+        s_rb[lane] = page * page_stride * rb;
+      }
+    }
+  }
+  for (int i = pfast ? n_pg : tid; i < n_pg; i += blockDim.x) {
     const int64_t pos = (pg0 + i) * P.ps > k0 ? (pg0 + i) * P.ps : k0;
     const int64_t slot = key_slot(P, R, b, pos);
     int64_t page = slot / P.ps;
@@ -678,6 +712,9 @@ __global__ void __launch_bounds__(NW * 32, (Smem<D, FP8, KM, NW>::kMinBlocks))
     }
   }
   cp_wait<0>();
+  // This CTA's reads are done: the next kernel on the stream may start its
+  // launch (its CTAs wait for this grid to finish before touching memory).
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   if constexpr (KM) {
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -852,7 +889,21 @@ cudaError_t launch_t(dim3 grid, const MmaParams &P, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(k_decode_mma<D, FP8, KM, NW>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k_decode_mma<D, FP8, KM, NW><<<grid, NW * 32, smem, s>>>(P);
+  // Programmatic dependent launch: this grid may be scheduled while the
+  // previous kernel on the stream finishes; the kernel waits for it before
+  // its first global access, so stream order is kept.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k_decode_mma<D, FP8, KM, NW>, P);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
