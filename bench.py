@@ -280,7 +280,7 @@ def run_native(args, rank, world):
         "tokens_per_s": round(spec.batch * world * K / (t_ms_max / 1e3), 1),
         "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(ach / peak, 4), "traffic": traffic,
-                     "kernel": "swa_attn_decode on full layers",
+                     "kernel": "swa_store_kv_attn_decode on full layers (k_decode_mma)",
                      "peak_source": peak_kind, "avg_launch_ms": round(full_attn_ms, 4)},
         "e2e": {"value": round(tot_e2e / (e2e_max / 1e3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -563,7 +563,7 @@ def spec_alloc_rate(st):
 # Sources of the dominant kernel of each bench line: its DRAM traffic, taken
 # from an ncu capture and stored under profiles/, is reported only while
 # these files are unchanged since the capture.
-DECODE_SOURCES = ("attn_decode_mma.cu", "split_merge.cuh", "swa_internal.h")
+DECODE_SOURCES = ("attn_decode_mma.cu", "split_merge.cuh", "kv_codec.cuh", "swa_internal.h")
 EXTEND_SOURCES = ("attn_extend_tc.cu", "swa_internal.h")
 
 
