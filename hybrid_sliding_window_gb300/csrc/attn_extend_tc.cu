@@ -472,12 +472,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ee < e_lo || ee > e_hi) rr[e] = 0xff800000u;   // -inf
         }
       };
-      // Pass 1: row maximum (S is read from TMEM twice instead of held in
-      // registers).  The 64-key loops stay rolled: one copy of each body
-      // keeps the softmax code inside the instruction cache.
-      float mx = -INFINITY;
+      // One pass over S, 64 keys at a time: each chunk's maximum is checked
+      // against the running reference maximum m_run, which moves only when a
+      // chunk exceeds it by more than kRescaleGap (weights stay below
+      // 2^kRescaleGap meanwhile).  A move rescales what was accumulated
+      // against the old reference - O of earlier tiles, the running sum and,
+      // for the second chunk, the first chunk's P already in TMEM - before
+      // this chunk's exponentials.  The 64-key loops stay rolled: one copy of
+      // each body keeps the softmax code inside the instruction cache.
+      const float sc = P.scale_log2;
+      const uint64_t sc2 = f2pack(sc, sc);
+      uint64_t acc2[2] = {0ull, 0ull};   // running pair sums (two chains)
 #pragma unroll 1
-      for (int cb = 0; cb < kKeys / 64; ++cb) {
+      for (int cb = 0; cb < 2; ++cb) {
         uint32_t rr[64];
         TC_LD32(tS + cb * 64, rr);        // two loads in flight before one wait
         TC_LD32(tS + cb * 64 + 32, (rr + 32));
@@ -488,41 +495,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 64; e += 2)
           m2[(e >> 1) & 3] = max3(m2[(e >> 1) & 3], __uint_as_float(rr[e]), __uint_as_float(rr[e + 1]));
-        mx = max3(mx, max3(m2[0], m2[1], m2[2]), m2[3]);
-      }
-      mx = mx == -INFINITY ? -INFINITY : mx * P.scale_log2;
-      // Lazy rescale: move the reference maximum only when it grows by more
-      // than kRescaleGap (weights stay below 2^kRescaleGap meanwhile).
-      float corr = 1.f;
-      if (mx > m_run + kRescaleGap || (m_run == -INFINITY && mx != -INFINITY)) {
-        corr = m_run == -INFINITY ? 0.f : exp2f(m_run - mx);
-        m_run = mx;
-      }
-      if (t > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-#pragma unroll 1
-        for (int cb = 0; cb < kD / 32; ++cb) {
-          uint32_t rr[32];
-          TC_LD32(tO + cb * 32, rr);
-          tc_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * corr);
-          TC_ST32(tO + cb * 32, rr);
+        float cm = max3(m2[0], m2[1], fmaxf(m2[2], m2[3]));
+        cm = cm == -INFINITY ? -INFINITY : cm * sc;
+        float corr = 1.f;
+        if (cm > m_run + kRescaleGap || (m_run == -INFINITY && cm != -INFINITY)) {
+          corr = m_run == -INFINITY ? 0.f : exp2f(m_run - cm);
+          m_run = cm;
         }
-      }
-      l_run *= corr;
-      const float mu = m_run == -INFINITY ? 0.f : m_run;
-      const float sc = P.scale_log2;
-      // Pass 2: P = exp2(scale*s - m) as packed bf16 pairs, written over the S
-      // columns already consumed (64-key half cb -> columns [32 cb, 32 cb + 32)).
-      const uint64_t sc2 = f2pack(sc, sc), nmu2 = f2pack(-mu, -mu);
-      uint64_t acc2[2] = {0ull, 0ull};   // running pair sums (two chains)
+        if (__any_sync(0xffffffffu, corr != 1.f)) {
+          if (t > 0) {
 #pragma unroll 1
-      for (int cb = 0; cb < 2; ++cb) {
-        uint32_t rr[64];
-        TC_LD32(tS + cb * 64, rr);
-        TC_LD32(tS + cb * 64 + 32, (rr + 32));
-        tc_wait_ld();
-        if (masked) mask_in_place(rr, cb);
+            for (int ob = 0; ob < kD / 32; ++ob) {
+              uint32_t ro[32];
+              TC_LD32(tO + ob * 32, ro);
+              tc_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * corr);
+              TC_ST32(tO + ob * 32, ro);
+            }
+          }
+          if (cb == 1) {
+            // the first chunk's P (32 columns of bf16 pairs) against the new reference
+            uint32_t pp[32];
+            tc_wait_st();
+            TC_LD32(tS, pp);
+            tc_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&pp[e]);
+              const float2 f = __bfloat1622float2(h);
+              h = __floats2bfloat162_rn(f.x * corr, f.y * corr);
+              pp[e] = *reinterpret_cast<uint32_t *>(&h);
+            }
+            TC_ST32(tS, pp);
+          }
+          float a0, a1, b0, b1;
+          f2unpack(acc2[0], a0, a1);
+          f2unpack(acc2[1], b0, b1);
+          acc2[0] = f2pack(a0 * corr, a1 * corr);
+          acc2[1] = f2pack(b0 * corr, b1 * corr);
+          l_run *= corr;
+        }
+        const float mu = m_run == -INFINITY ? 0.f : m_run;
+        const uint64_t nmu2 = f2pack(-mu, -mu);
+        // P = exp2(scale*s - m) as packed bf16 pairs, written over the S
+        // columns already consumed (64-key chunk cb -> columns [32 cb, 32 cb + 32)).
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
