@@ -222,31 +222,99 @@ def run_native(args, rank, world):
     assert api.swa_device_check(st.ctx) == 0, "device-side check flagged an error"
 
     # e2e: the same steps fed from pinned host memory, outputs copied back.
+    # A step's inputs (q, k, v of every layer and the lengths) travel as one
+    # pinned buffer and one copy, the outputs of every layer come back as one
+    # copy; the copies run on their own stream with double-buffered device
+    # buffers, so step s+1's inputs and step s's outputs move while the GPU
+    # computes step s.
+    B = st.B
+    parts = [(key, l) for key in ("q", "k", "v") for l in range(len(inputs[0][key]))]
+    layout, off = {}, 0
+    for key, l in parts:
+        t = inputs[0][key][l]
+        layout[(key, l)] = (off, tuple(t.shape), t.dtype, t.numel() * t.element_size())
+        off += (t.numel() * t.element_size() + 255) // 256 * 256
+    for key in ("seq", "pre"):
+        layout[key] = off
+        off += (B * 8 + 255) // 256 * 256
+    in_bytes = off
+
+    def in_views(buf):
+        d = {"q": [], "k": [], "v": []}
+        for key, l in parts:
+            o, shape, dt, n = layout[(key, l)]
+            d[key].append(buf[o:o + n].view(dt).view(shape))
+        for key in ("seq", "pre"):
+            d[key] = buf[layout[key]:layout[key] + B * 8].view(torch.int64)
+        return d
+
     host_in = []
     for s in range(K):
-        inp = inputs[W + K + s]
-        host_in.append({key: [t.cpu().pin_memory() for t in inp[key]] for key in ("q", "k", "v")})
-    dev_in = {key: [torch.empty_like(t) for t in inputs[0][key]] for key in ("q", "k", "v")}
-    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in st.outs]
-    h2d = sum(t.numel() * t.element_size() for key in ("q", "k", "v") for t in dev_in[key])
-    d2h = sum(o.numel() * o.element_size() for o in st.outs)
+        src = inputs[W + K + s]
+        hb = torch.empty(in_bytes, dtype=torch.uint8, pin_memory=True)
+        hv = in_views(hb)
+        for key, l in parts:
+            hv[key][l].copy_(src[key][l].cpu())
+        hv["seq"].copy_(torch.from_numpy(np.asarray(src["seq_h"], np.int64)))
+        hv["pre"].copy_(torch.from_numpy(np.asarray(src["pre_h"], np.int64)))
+        host_in.append(hb)
+    dev_buf = [torch.empty(in_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    dev_in = [in_views(b) for b in dev_buf]
+    o_sizes = [o.numel() * o.element_size() for o in st.outs]
+    out_bytes = sum(o_sizes)
+    out_flat = [torch.empty(out_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    out_sets = []
+    for fb in out_flat:
+        views, o = [], 0
+        for t, n in zip(st.outs, o_sizes):
+            views.append(fb[o:o + n].view(t.dtype).view(t.shape))
+            o += n
+        out_sets.append(views)
+    host_out = [torch.empty(out_bytes, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+    h2d, d2h = in_bytes, out_bytes
+    outs_saved = st.outs
+    cs = torch.cuda.current_stream()
+    ps = torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    in_ready, in_free = [ev(), ev()], [ev(), ev()]
+    out_ready, out_free = [ev(), ev()], [ev(), ev()]
     e2e_bytes = 0
     barrier()
     x0 = torch.cuda.Event(enable_timing=True)
     x1 = torch.cuda.Event(enable_timing=True)
-    x0.record()
+    x0.record(cs)
+    ps.wait_event(x0)
+    with torch.cuda.stream(ps):
+        dev_buf[0].copy_(host_in[0], non_blocking=True)
+        in_ready[0].record(ps)
     for s in range(K):
+        i = s % 2
+        if s + 1 < K:                      # next step's inputs, behind this step's compute
+            j = (s + 1) % 2
+            with torch.cuda.stream(ps):
+                if s >= 1:
+                    ps.wait_event(in_free[j])
+                dev_buf[j].copy_(host_in[s + 1], non_blocking=True)
+                in_ready[j].record(ps)
+        cs.wait_event(in_ready[i])
+        if s >= 2:
+            cs.wait_event(out_free[i])     # step s-2's outputs have left this buffer
         src = inputs[W + K + s]
-        for key in ("q", "k", "v"):
-            for d_, h_ in zip(dev_in[key], host_in[s][key]):
-                d_.copy_(h_, non_blocking=True)
-        step_inp = dict(src, q=dev_in["q"], k=dev_in["k"], v=dev_in["v"])
+        d = dev_in[i]
+        st.outs = out_sets[i]
         e2e_bytes += st.kv_bytes_per_step(src["seq_h"])["total"]
-        st.decode_step(step_inp)
-        for h_, o in zip(host_out, st.outs):
-            h_.copy_(o, non_blocking=True)
-    x1.record()
+        st.decode_step(dict(q=d["q"], k=d["k"], v=d["v"], seq_h=src["seq_h"], pre_h=src["pre_h"],
+                            seq_d=d["seq"], pre_d=d["pre"]))
+        in_free[i].record(cs)
+        out_ready[i].record(cs)
+        with torch.cuda.stream(ps):
+            ps.wait_event(out_ready[i])
+            host_out[i].copy_(out_flat[i], non_blocking=True)
+            out_free[i].record(ps)
+    cs.wait_stream(ps)
+    x1.record(cs)
     barrier()
+    st.outs = outs_saved
     e2e_ms = x0.elapsed_time(x1)
     assert api.swa_device_check(st.ctx) == 0
     spec_alloc = spec_alloc_rate(st) if rank == 0 else None
@@ -283,7 +351,10 @@ def run_native(args, rank, world):
                      "kernel": "swa_store_kv_attn_decode on full layers (k_decode_mma)",
                      "peak_source": peak_kind, "avg_launch_ms": round(full_attn_ms, 4)},
         "e2e": {"value": round(tot_e2e / (e2e_max / 1e3) / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "copies": "per step one pinned host-to-device copy of q/k/v and lengths, one "
+                          "device-to-host copy of all outputs, on a copy stream overlapped with "
+                          "the previous / next step's compute"},
         "clocks": clocks,
         "gpu_launches": st.launches_per_step() * K,
         "attn_path": api.swa_last_attn_path(st.ctx),
