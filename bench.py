@@ -195,7 +195,7 @@ def run_native(args, rank, world):
         torch.cuda.synchronize()
 
     for s in range(W):
-        st.decode_step(inputs[s])
+        st.decode_step(inputs[s], fused=not args.separate_store)
     full_layers = [l for l, (k, _, _) in enumerate(spec.layers) if k == FULL]
     ev = {l: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(K)] for l in full_layers}
@@ -212,7 +212,7 @@ def run_native(args, rank, world):
         b = st.kv_bytes_per_step(inp["seq_h"])
         bytes_steps.append(b["total"])
         attn_bytes.append(b["full"] / len(full_layers))
-        st.decode_step(inp, {l: ev[l][s] for l in full_layers})
+        st.decode_step(inp, {l: ev[l][s] for l in full_layers}, fused=not args.separate_store)
     e1.record()
     barrier()
     clocks = clk.stop()
@@ -304,7 +304,7 @@ def run_native(args, rank, world):
         st.outs = out_sets[i]
         e2e_bytes += st.kv_bytes_per_step(src["seq_h"])["total"]
         st.decode_step(dict(q=d["q"], k=d["k"], v=d["v"], seq_h=src["seq_h"], pre_h=src["pre_h"],
-                            seq_d=d["seq"], pre_d=d["pre"]))
+                            seq_d=d["seq"], pre_d=d["pre"]), fused=not args.separate_store)
         in_free[i].record(cs)
         out_ready[i].record(cs)
         with torch.cuda.stream(ps):
@@ -341,6 +341,8 @@ def run_native(args, rank, world):
                    "kv_bytes_per_step": int(sum(bytes_steps) / K),
                    "l2": "no flush: each step reads far more KV than the 129 MB L2",
                    "pools_tokens": {"full": st.size_full, "swa": st.size_swa},
+                   "kv_store": ("separate swa_store_kv launch" if args.separate_store
+                                else "inside the attention launch (swa_store_kv_attn_decode)"),
                    "swa_pool": (f"per-request ring of {st.ring_size} tokens" if st.swa_ring
                                 else "paged"),
                    "setup_s": round(setup_s, 1)},
@@ -697,6 +699,9 @@ def main():
     ap.add_argument("--workload", default="mimo",
                     choices=["mimo", "gptoss", "llama4", "extend", "radix"])
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--separate-store", action="store_true",
+                    help="decode steps call swa_store_kv and swa_attn_decode separately instead of "
+                         "swa_store_kv_attn_decode")
     ap.add_argument("--no-extend", action="store_true",
                     help="skip the extend / evict figures added to the decode line")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
