@@ -105,9 +105,10 @@ class Pair:
         return t.to(torch.bfloat16) if self.dtype != "f32" else t
 
     # -------------------------------------------------------------- steps ---
-    def extend(self, rows, pre, seq, check_alloc=True):
+    def extend(self, rows, pre, seq, check_alloc=True, store=True):
         """Allocate + store positions pre..seq-1 of request rows (row ids of
-        req_to_token; request id for the generator = row)."""
+        req_to_token; request id for the generator = row).  store=False
+        allocates only (a decode step whose attention call stores the token)."""
         rows = list(rows)
         pre = np.asarray(pre, np.int64)
         seq = np.asarray(seq, np.int64)
@@ -132,7 +133,9 @@ class Pair:
             if check_alloc:
                 np.testing.assert_array_equal(out_f.cpu().numpy(), np.array(of, np.int64))
                 np.testing.assert_array_equal(out_s.cpu().numpy(), np.array(osw, np.int64))
-        for l in range(len(self.layers)):
+        if self.oracle:
+            self.last_alloc = (of, osw)
+        for l in range(len(self.layers) if store else 0):
             k, v = self.kv_in(l, reqs, pos)
             api.swa_store_kv(self.ctx, l, self.to_dev(k), self.to_dev(v), out_f, out_s,
                              self.k_scale, self.v_scale)
@@ -157,8 +160,11 @@ class Pair:
             np.testing.assert_array_equal(np.array(o_ev, np.int64), evicted_h)
         return evicted_h
 
-    def decode_attention(self, rows, seq, layers=None, max_seq_len=None):
-        """Query at seq-1 (KV stored).  Returns {layer: (gpu, oracle)}."""
+    def decode_attention(self, rows, seq, layers=None, max_seq_len=None, new_slots=None):
+        """Query at seq-1 (KV stored).  Returns {layer: (gpu, oracle)}.
+        new_slots=(out_f, out_s) from extend(..., store=False): the token at
+        seq-1 is not stored yet; each layer's swa_store_kv_attn_decode stores
+        it (the oracle stores it first)."""
         rows = list(rows)
         seq = np.asarray(seq, np.int64)
         bs = len(rows)
@@ -174,8 +180,19 @@ class Pair:
             out = torch.empty_like(qd)
             ws = torch.zeros(api.swa_attn_decode_ws_bytes(self.ctx, l, bs, msl), dtype=torch.uint8,
                              device="cuda")
-            api.swa_attn_decode(self.ctx, l, self.rt, d_rows, d_seq, msl, plan, qd, self.sinks_d[l],
-                                self.scale, out, ws, self.k_scale, self.v_scale)
+            if new_slots is None:
+                api.swa_attn_decode(self.ctx, l, self.rt, d_rows, d_seq, msl, plan, qd,
+                                    self.sinks_d[l], self.scale, out, ws, self.k_scale,
+                                    self.v_scale)
+            else:
+                k, v = self.kv_in(l, rows, list(seq - 1))
+                if self.oracle:
+                    of, osw = self.last_alloc
+                    self.op.store(l, k, v, of, osw, self.k_scale, self.v_scale)
+                api.swa_store_kv_attn_decode(self.ctx, l, self.rt, d_rows, d_seq, msl, plan, qd,
+                                             self.to_dev(k), self.to_dev(v), new_slots[0],
+                                             new_slots[1], self.sinks_d[l], self.scale, out, ws,
+                                             self.k_scale, self.v_scale)
             g = out.float().cpu().numpy()
             o = None
             if self.oracle:

@@ -91,3 +91,30 @@ def test_fused_out_of_range_slot_flags_and_skips():
     torch.cuda.synchronize()
     assert api.swa_device_check(st.ctx) & 4                # SWA_DEVERR_RANGE
     assert torch.equal(k_before.view(torch.int16), st.kv[l][0].view(torch.int16))
+
+
+@pytest.mark.parametrize("dtype,D,G", [("bf16", 128, 16), ("bf16", 64, 4), ("e4m3", 128, 5),
+                                       ("f32", 64, 2)])
+def test_fused_against_oracle(dtype, D, G):
+    """The fused call straight against the oracle (store, then attention over
+    the tables), through chunked prefill with eviction: the tensor-core kernel
+    for bf16 / E4M3 pools, the generic path (store kernel first) for f32."""
+    from oracle import attention as OT
+    from tests.harness import Pair, TOL, assert_close
+    scales = dict(k_scale=0.37, v_scale=1.9) if dtype == "e4m3" else {}
+    P = Pair([(OT.SLIDING, 31, 2), (OT.FULL, 0, 2), (OT.CHUNKED, 64, 2)], Hq=2 * G, D=D,
+             dtype=dtype, ps=16, size_full=4096, size_swa=1024, perm_free=True, seed=11, **scales)
+    rows = [1, 2, 3, 4]
+    lens = np.zeros(4, np.int64)
+    ev = np.zeros(4, np.int64)
+    for chunk in ([100, 37, 1, 260], [60, 5, 130, 80]):
+        P.evict(rows, lens, ev, 0)
+        P.extend(rows, lens, lens + np.array(chunk))
+        lens = lens + np.array(chunk)
+    for _ in range(3):                                   # decode steps
+        P.evict(rows, lens, ev, 8)
+        slots = P.extend(rows, lens, lens + 1, store=False)
+        lens = lens + 1
+        P.check_state()
+        for l, (g, o) in P.decode_attention(rows, lens, new_slots=slots).items():
+            assert_close(g, o, TOL[dtype], f"fused {dtype} layer {l}")
