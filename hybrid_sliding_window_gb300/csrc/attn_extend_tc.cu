@@ -387,23 +387,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Order per tile t: O0(t), S0(t+1), O1(t), S1(t+1) - softmax group 0 works
     // on tile t+1 while the tensor core runs O1(t) and S1(t+1), and group 1
     // likewise one slot later.
+    // Shared-memory descriptors built once per tile and stage: a K step only
+    // advances the 14-bit address field by (byte offset >> 4), which cannot
+    // carry out of the field (shared addresses stay below 256 KB), so each
+    // product's descriptors are one add from these.
+    const uint64_t dq0 = smem_desc(sb + kOffQ, 16, 1024);
+    const uint64_t dq1 = smem_desc(sb + kOffQ + kTileBytes, 16, 1024);
+    const uint64_t dk0 = smem_desc(sb + kOffK, 16, 1024);
+    const uint64_t dk1 = smem_desc(sb + kOffK + kTileBytes, 16, 1024);
+    const uint64_t dv0 = smem_desc(sb + kOffV, kHalf, 1024);
+    const uint64_t dv1 = smem_desc(sb + kOffV + kTileBytes, kHalf, 1024);
     auto issue_s = [&](int i, int t) {
-      const uint32_t qa = sb + kOffQ + i * kTileBytes;
-      const uint32_t kt = sb + kOffK + (t & 1) * kTileBytes;
+      const uint64_t qd = i ? dq1 : dq0, kd = (t & 1) ? dk1 : dk0;
 #pragma unroll
       for (int ks = 0; ks < kD / 16; ++ks) {
-        const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
-        mma_ss(tmem + i * 128, smem_desc(qa + off, 16, 1024), smem_desc(kt + off, 16, 1024), kIdS,
-               ks > 0);
+        const uint64_t off16 = ((ks >> 2) * kHalf + (ks & 3) * 32) >> 4;
+        mma_ss(tmem + i * 128, qd + off16, kd + off16, kIdS, ks > 0);
       }
       tc_commit(bar(B_SDONE + i));
     };
     auto issue_o = [&](int i, int t) {
-      const uint32_t vt = sb + kOffV + (t & 1) * kTileBytes;
+      const uint64_t vd = (t & 1) ? dv1 : dv0;
 #pragma unroll
       for (int ks = 0; ks < kKeys / 16; ++ks)
-        mma_ts(tmem + 256 + i * 128, tmem + i * 128 + ks * 8,
-               smem_desc(vt + ks * 16 * 128, kHalf, 1024), kIdO, (t > 0 || ks > 0) ? 1u : 0u);
+        mma_ts(tmem + 256 + i * 128, tmem + i * 128 + ks * 8, vd + (uint64_t)(ks * 16 * 128 >> 4),
+               kIdO, (t > 0 || ks > 0) ? 1u : 0u);
     };
     if (lane == 0 && mbar_wait(bar(B_FULLK + 0), 0, &s_abort)) {
       tc_fence_after();
