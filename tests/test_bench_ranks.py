@@ -3,7 +3,6 @@ own replica; the job's time is the maximum over ranks and its work the sum."""
 import os
 import socket
 
-import pytest
 import torch
 import torch.distributed as tdist
 import torch.multiprocessing as mp

@@ -15,11 +15,8 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():
     pytest.skip("needs a GPU", allow_module_level=True)
 
-from hybrid_sliding_window_gb300 import api, synth  # noqa: E402
+from hybrid_sliding_window_gb300 import api  # noqa: E402
 from hybrid_sliding_window_gb300.workloads import SPECS, DecodeState, FULL, SLIDING, CHUNKED  # noqa: E402
-from oracle import allocator as OA  # noqa: E402
-from oracle import attention as OT  # noqa: E402
-from oracle import codecs as OC  # noqa: E402
 from tests.harness import TOL, assert_close, check_state, oracle_decode, replay  # noqa: E402
 
 def run_small(spec, steps=3, layers=None, requests=None, path=-1, expect_path=None):
