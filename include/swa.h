@@ -432,7 +432,11 @@ swa_status swa_plan(swa_ctx *ctx, int32_t bs, const int32_t *req_to_token,
  * path extend call with more query tokens than max_batch needs its own.
  *
  * swa_attn_decode: one query per request at p = seq_lens[b] - 1 (its KV
- * already stored). max_seq_len bounds seq_lens (host; sizes the grid). */
+ * already stored). max_seq_len bounds seq_lens (host; sizes the grid).  On
+ * the tensor-core path the launch is a programmatic dependent of the kernel
+ * before it on the stream: it may be scheduled while that kernel finishes,
+ * but reads nothing until that kernel has completed, so stream order and
+ * every input the previous kernel wrote are respected as for a plain launch. */
 size_t swa_attn_decode_ws_bytes(const swa_ctx *ctx, int32_t layer, int32_t bs,
                                 int32_t max_seq_len);
 swa_status swa_attn_decode(swa_ctx *ctx, int32_t layer, int32_t bs,
