@@ -201,6 +201,7 @@ def run_native(args, rank, world):
               for _ in range(K)] for l in full_layers}
     bytes_steps = []
     attn_bytes = []
+    launches = 0          # kernel launches of this library inside the timed region
     barrier()
     clk = ClockSampler(local)
     clk.start()
@@ -213,6 +214,7 @@ def run_native(args, rank, world):
         bytes_steps.append(b["total"])
         attn_bytes.append(b["full"] / len(full_layers))
         st.decode_step(inp, {l: ev[l][s] for l in full_layers}, fused=not args.separate_store)
+        launches += st.launches_per_step()
     e1.record()
     barrier()
     clocks = clk.stop()
@@ -358,7 +360,7 @@ def run_native(args, rank, world):
                           "device-to-host copy of all outputs, on a copy stream overlapped with "
                           "the previous / next step's compute"},
         "clocks": clocks,
-        "gpu_launches": st.launches_per_step() * K,
+        "gpu_launches": launches,
         "attn_path": api.swa_last_attn_path(st.ctx),
         "spec_alloc": spec_alloc,
         "translate_for_kernel": kernel_ids,

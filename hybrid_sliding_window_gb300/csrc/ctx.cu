@@ -514,9 +514,13 @@ swa_status swa_evict_swa(swa_ctx *c, int32_t bs, const int32_t *rt, int64_t rt_s
       new_ev[b] = nw;
     }
   }
-  CUDA_TRY(c, swa::launch_evict(*c, bs, rt, rt_stride, req_idx, pre_lens, evicted,
-                                protected_lens, interval, radix, kEvictMaxPages,
-                                (cudaStream_t)stream));
+  // The host lengths decide exactly what the kernels would do (the lengths
+  // travel with their device copies); a call that evicts nothing (most decode
+  // steps between interval triggers) launches nothing.
+  if (total > 0)
+    CUDA_TRY(c, swa::launch_evict(*c, bs, rt, rt_stride, req_idx, pre_lens, evicted,
+                                  protected_lens, interval, radix, kEvictMaxPages,
+                                  (cudaStream_t)stream));
   if (!c->ring_cost) mirror_release(c, false, total);
   std::copy(new_ev.begin(), new_ev.end(), evicted_h);
   return SWA_OK;

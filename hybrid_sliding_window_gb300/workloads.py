@@ -196,6 +196,7 @@ class DecodeState:
         self.scale = 1.0 / math.sqrt(spec.D)
         self.in_dtype = torch.float32 if spec.dtype == "f32" else torch.bfloat16
         self.stream = torch.cuda.current_stream()
+        self.last_launches = 0
 
     # -- helpers ------------------------------------------------------------
     def _synth(self, stream_id, layer, req_d, pos_d, heads):
@@ -309,8 +310,10 @@ class DecodeState:
         if self.trace is not None:
             self.trace.append(("evict", self.rows.tolist(), inp["pre_h"].tolist(),
                                self.evicted.tolist(), spec.interval))
+        ev_before = self.evicted.copy()
         api.swa_evict_swa(self.ctx, self.rt, self.rows_d, inp["pre_d"], self.evicted_d,
                           inp["pre_h"], self.evicted, interval=spec.interval)
+        launches = 3 if (self.evicted != ev_before).any() else 0
         if self.trace is not None:
             self.trace.append(("decode", self.rows.tolist(), inp["seq_h"].tolist()))
         api.swa_alloc_decode(self.ctx, inp["seq_d"], None, inp["seq_h"], self.out_full,
@@ -337,6 +340,8 @@ class DecodeState:
                                     self.outs[l], self.ws)
             if ev is not None:
                 ev[1].record()
+            launches += 1 if fused and api.swa_last_attn_path(self.ctx) == 1 else 2
+        self.last_launches = launches + 2 + 1      # + alloc_decode, plan
         self.lens = inp["seq_h"].copy()
 
     # -- extend (one chunked-prefill round) -------------------------------------
@@ -413,8 +418,11 @@ class DecodeState:
         return {"full": full, "swa": swa, "total": full + swa}
 
     def launches_per_step(self) -> int:
-        # evict (3) + alloc_decode (2) + plan (1) + per layer store (1) + attention (1)
-        return 3 + 2 + 1 + 2 * len(self.spec.layers)
+        """Kernel launches of the last decode_step: eviction (3, only when a
+        request evicts), alloc_decode (2), plan (1), and per layer the store and
+        the attention (one launch when the tensor-core decode kernel stores the
+        token itself)."""
+        return self.last_launches
 
     def kv_bytes_per_step(self, seq_h=None) -> dict:
         """Algorithmic K+V bytes read by attention in one decode step."""

@@ -377,7 +377,8 @@ swa_status swa_free_swa(swa_ctx *ctx, const int64_t *full_idx, int64_t n,
  * ones - the order of per-request frees), their mapping entries set to 0,
  * and evicted[b] = new.  Device arrays drive the kernel; the *_host arrays
  * (same values) drive the host mirror, and evicted_host is updated too.
- * protected may be NULL (all 0). */
+ * When the host arrays show that no request frees a page, no kernel is
+ * launched.  protected may be NULL (all 0). */
 swa_status swa_evict_swa(swa_ctx *ctx, int32_t bs, const int32_t *req_to_token,
                          int64_t rt_stride, const int64_t *req_idx,
                          const int64_t *pre_lens, int64_t *evicted,
