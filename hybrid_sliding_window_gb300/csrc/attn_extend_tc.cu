@@ -33,6 +33,8 @@
 // reason.
 // Every mbarrier wait has a poll limit; on expiry the kernel sets an error
 // bit, every role leaves its loop, and the TMEM is still released.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -258,42 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int T = kRows / G;                 // tokens per Q tile
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
-  // ---- work item: two Q tiles of one request, latest first ----
-  if (tid == 0) {
-    int64_t tau = (int64_t)P.items_upper - 1 - blockIdx.x, acc = 0;
-    s_req = -1;
-    for (int b = 0; b < P.bs; ++b) {
-      const int64_t ext = P.qo_indptr[b + 1] - P.qo_indptr[b];
-      const int64_t n = (ext + 2 * T - 1) / (2 * T);
-      if (tau < acc + n) {
-        const int64_t local = (tau - acc) * 2 * T;
-        s_req = b;
-        s_q0 = P.qo_indptr[b] + local;
-        s_qend = P.qo_indptr[b + 1];
-        s_pfirst = P.pre[b] + local;
-        break;
-      }
-      acc += n;
-    }
-    s_abort = 0;
-  }
-  __syncthreads();
-  if (s_req < 0) return;
-  const int b = (int)s_req;
-  const int64_t q0 = s_q0, n_tok = min((int64_t)2 * T, s_qend - s_q0);
-  const int64_t p_first = s_pfirst, p_last = p_first + n_tok - 1;
-  const int64_t k_lo = key_lo(P.kind, P.window, p_first);
-  const int64_t k_hi = p_last;
-  const int64_t kt0 = (k_lo / kKeys) * kKeys;      // key tiles are 128-aligned
-  const int n_tiles = (int)((k_hi - kt0) / kKeys + 1);
-  const int64_t pg0 = kt0 / P.ps;
-  const int n_pg = (int)(k_hi / P.ps - pg0 + 1);
-  if (n_pg > P.max_pages || n_tiles * (kKeys / P.ps) > P.max_pages) {
-    if (tid == 0) set_error(P.err, SWA_DEVERR_RANGE);
-    return;
-  }
-
-  // ---- set-up: TMEM, barriers, page rows, zeroed K/V stages ----
+  // ---- once per CTA: TMEM, barriers ----
+  if (tid == 0) s_abort = 0;
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
                      smem_u32(&s_tmem)),
@@ -312,6 +280,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_ODONE), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  constexpr uint32_t kIdS = idesc_f16(128, 128, false);
+  constexpr uint32_t kIdO = idesc_f16(128, 128, true);
+
+  // Persistent: the CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...
+  // Every barrier phase follows the CTA's running tile count tg0 (key tiles
+  // of its earlier items) or item count n_done, so the rings run on across
+  // items; each item ends with all roles joined (its Q tiles and TMEM free).
+  int tg0 = 0, n_done = 0;
+  for (int item = blockIdx.x; item < P.items_upper; item += gridDim.x) {
+  __syncthreads();   // every thread has read the previous item's fields
+  // ---- work item: two Q tiles of one request, latest first ----
+  if (tid == 0) {
+    int64_t tau = (int64_t)P.items_upper - 1 - item, acc = 0;
+    s_req = -1;
+    for (int b = 0; b < P.bs; ++b) {
+      const int64_t ext = P.qo_indptr[b + 1] - P.qo_indptr[b];
+      const int64_t n = (ext + 2 * T - 1) / (2 * T);
+      if (tau < acc + n) {
+        const int64_t local = (tau - acc) * 2 * T;
+        s_req = b;
+        s_q0 = P.qo_indptr[b] + local;
+        s_qend = P.qo_indptr[b + 1];
+        s_pfirst = P.pre[b] + local;
+        break;
+      }
+      acc += n;
+    }
+  }
+  __syncthreads();
+  if (s_req < 0) continue;
+  const int b = (int)s_req;
+  const int64_t q0 = s_q0, n_tok = min((int64_t)2 * T, s_qend - s_q0);
+  const int64_t p_first = s_pfirst, p_last = p_first + n_tok - 1;
+  const int64_t k_lo = key_lo(P.kind, P.window, p_first);
+  const int64_t k_hi = p_last;
+  const int64_t kt0 = (k_lo / kKeys) * kKeys;      // key tiles are 128-aligned
+  const int n_tiles = (int)((k_hi - kt0) / kKeys + 1);
+  const int64_t pg0 = kt0 / P.ps;
+  const int n_pg = (int)(k_hi / P.ps - pg0 + 1);
+  if (n_pg > P.max_pages || n_tiles * (kKeys / P.ps) > P.max_pages) {
+    if (tid == 0) set_error(P.err, SWA_DEVERR_RANGE);
+    continue;
+  }
+
   // Q rows of both tiles, gathered by every thread (cp.async, zero fill past
   // the chunk); their latency overlaps the page-row lookups below.
   {
@@ -357,18 +372,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_async_smem();   // Q (written by cp.async) is read by the tensor core
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = s_tmem;
-  constexpr uint32_t kIdS = idesc_f16(128, 128, false);
-  constexpr uint32_t kIdO = idesc_f16(128, 128, true);
 
   if (warp == 9) {
     // ===================== producer: K/V pages =====================
     if (lane == 0) {
       const int pages_per_tile = kKeys / P.ps;
       for (int t = 0; t < n_tiles && !s_abort; ++t) {
-        const int s = t & 1;
+        const int T = tg0 + t;             // the CTA's running tile count
+        const int s = T & 1;
         for (int kv = 0; kv < 2; ++kv) {
-          if (t >= 2 && !mbar_wait(bar((kv ? B_EMPTYV : B_EMPTYK) + s), ((t >> 1) - 1) & 1, &s_abort))
+          if (T >= 2 && !mbar_wait(bar((kv ? B_EMPTYV : B_EMPTYK) + s), ((T >> 1) - 1) & 1, &s_abort))
             break;
           const uint32_t full = bar((kv ? B_FULLV : B_FULLK) + s);
           mbar_expect_tx(full, (uint32_t)kTileBytes);   // every page slot is loaded
@@ -397,8 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dk1 = smem_desc(sb + kOffK + kTileBytes, 16, 1024);
     const uint64_t dv0 = smem_desc(sb + kOffV, kHalf, 1024);
     const uint64_t dv1 = smem_desc(sb + kOffV + kTileBytes, kHalf, 1024);
-    auto issue_s = [&](int i, int t) {
-      const uint64_t qd = i ? dq1 : dq0, kd = (t & 1) ? dk1 : dk0;
+    auto issue_s = [&](int i, int T) {     // T: running tile count (stage)
+      const uint64_t qd = i ? dq1 : dq0, kd = (T & 1) ? dk1 : dk0;
 #pragma unroll
       for (int ks = 0; ks < kD / 16; ++ks) {
         const uint64_t off16 = ((ks >> 2) * kHalf + (ks & 3) * 32) >> 4;
@@ -406,36 +419,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_commit(bar(B_SDONE + i));
     };
-    auto issue_o = [&](int i, int t) {
-      const uint64_t vd = (t & 1) ? dv1 : dv0;
+    auto issue_o = [&](int i, int t, int T) {   // t: tile of the item, T: running count
+      const uint64_t vd = (T & 1) ? dv1 : dv0;
 #pragma unroll
       for (int ks = 0; ks < kKeys / 16; ++ks)
         mma_ts(tmem + 256 + i * 128, tmem + i * 128 + ks * 8, vd + (uint64_t)(ks * 16 * 128 >> 4),
                kIdO, (t > 0 || ks > 0) ? 1u : 0u);
     };
-    if (lane == 0 && mbar_wait(bar(B_FULLK + 0), 0, &s_abort)) {
+    if (lane == 0 && mbar_wait(bar(B_FULLK + (tg0 & 1)), (tg0 >> 1) & 1, &s_abort)) {
       tc_fence_after();
-      issue_s(0, 0);
-      issue_s(1, 0);
-      tc_commit(bar(B_EMPTYK + 0));
+      issue_s(0, tg0);
+      issue_s(1, tg0);
+      tc_commit(bar(B_EMPTYK + (tg0 & 1)));
       for (int t = 0; t < n_tiles; ++t) {
-        const int s = t & 1, s1 = (t + 1) & 1;
+        const int T = tg0 + t;
+        const int s = T & 1, s1 = (T + 1) & 1;
         const bool more = t + 1 < n_tiles;
-        if (!mbar_wait(bar(B_FULLV + s), (t >> 1) & 1, &s_abort)) break;
-        if (!mbar_wait(bar(B_PREADY + 0), t & 1, &s_abort)) break;
+        if (!mbar_wait(bar(B_FULLV + s), (T >> 1) & 1, &s_abort)) break;
+        if (!mbar_wait(bar(B_PREADY + 0), T & 1, &s_abort)) break;
         tc_fence_after();
-        issue_o(0, t);
+        issue_o(0, t, T);
         if (more) {
-          if (!mbar_wait(bar(B_FULLK + s1), ((t + 1) >> 1) & 1, &s_abort)) break;
+          if (!mbar_wait(bar(B_FULLK + s1), ((T + 1) >> 1) & 1, &s_abort)) break;
           tc_fence_after();
-          issue_s(0, t + 1);
+          issue_s(0, T + 1);
         }
-        if (!mbar_wait(bar(B_PREADY + 1), t & 1, &s_abort)) break;
+        if (!mbar_wait(bar(B_PREADY + 1), T & 1, &s_abort)) break;
         tc_fence_after();
-        issue_o(1, t);
+        issue_o(1, t, T);
         tc_commit(bar(B_EMPTYV + s));
         if (more) {
-          issue_s(1, t + 1);
+          issue_s(1, T + 1);
           tc_commit(bar(B_EMPTYK + s1));
         }
       }
@@ -456,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool alive = true;
     for (int t = 0; t < n_tiles; ++t) {
       // Warp-uniform outcome: the TMEM loads below are warp-collective.
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_SDONE + grp), t & 1, &s_abort))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_SDONE + grp), (tg0 + t) & 1, &s_abort))) {
         alive = false;
         break;
       }
@@ -573,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(B_PREADY + grp));
     }
     // ---- epilogue ----
-    if (alive && __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), 0, &s_abort))) {
+    if (alive && __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), n_done & 1, &s_abort))) {
       tc_fence_after();
       float sg2 = -INFINITY;
       if (P.sinks) sg2 = P.sinks[kvh * G + g] * 1.4426950408889634f;
@@ -619,6 +633,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+  }
+  // end of the item: all roles joined before its Q tiles and TMEM are reused
+  tc_fence_before();
+  __syncthreads();
+  tg0 += n_tiles;
+  ++n_done;
+  if (s_abort) break;
+  tc_fence_after();
   }
   if (s_abort && tid == 0) set_error(P.err, SWA_DEVERR_RANGE);
   tc_fence_before();
@@ -673,7 +695,10 @@ cudaError_t launch_attn_extend_tc(Ctx &c, const AttnArgs &a, cudaStream_t s) {
   cudaError_t e =
       cudaFuncSetAttribute(k_extend_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(P.items_upper, L.hkv);
+  // Persistent: one CTA per SM (the KV heads share the SMs), each looping
+  // over its items.
+  const int per_head = std::max(1, (c.num_sms > 0 ? c.num_sms : 148) / L.hkv);
+  dim3 grid(std::min(P.items_upper, per_head), L.hkv);
   k_extend_tc<<<grid, kThreads, smem, s>>>(L.tmk, L.tmv, P);
   return cudaGetLastError();
 }
