@@ -6,8 +6,10 @@
 // pre..seq-1 attend causally; sliding layers see the last Wx+1 keys, full
 // layers every earlier key; a per-head sink joins the denominator.
 //
-// GB300 design (one CTA per SM, 10 warps, warp-specialised):
-//   * the CTA owns two 128-row Q tiles, each (128/G) consecutive query tokens
+// GB300 design (persistent: one CTA per SM loops over work items; 10 warps,
+// warp-specialised; TMEM and barriers set up once per CTA, barrier phases
+// following the CTA's running tile count across items):
+//   * an item is two 128-row Q tiles, each (128/G) consecutive query tokens
 //     x the G query heads of one KV head, so every K/V tile it loads feeds two
 //     QK^T and two PV products;
 //   * all threads gather the Q rows once (cp.async) while the page rows are
