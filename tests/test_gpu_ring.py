@@ -5,8 +5,10 @@ Chunked prefill (chunks bounded by ring cost - lookback) then decode steps,
 with the eviction pass and request frees in between: ring slots, mapping,
 full free list, req_to_token and stored KV bytes bit for bit after every
 step; decode and extend attention within the dtype tolerance, through the
-generic kernel (f32, D = 32) and through the tensor-core kernels (bf16,
-D = 128, G = 8: keys-as-rows decode and tcgen05 extend).  Plus the calls and
+generic kernel (f32, D = 32), through the tensor-core kernels (bf16,
+D = 128, G = 8: keys-as-rows decode and tcgen05 extend) and with E4M3 pools in
+the page-major envelope on chunked-local layers (G = 5); every other decode
+step stores its new token inside the attention call.  Plus the calls and
 configurations ring mode rejects."""
 import numpy as np
 import pytest
@@ -26,13 +28,18 @@ CASES = {
     # name: (layers, Hq, D, dtype, ps, ring_size, chunk)
     "f32_generic": ([(OT.SLIDING, 7, 1), (OT.FULL, 0, 1)], 2, 32, "f32", 4, 20, 12),
     "bf16_tensor_core": ([(OT.SLIDING, 127, 2), (OT.FULL, 0, 2)], 16, 128, "bf16", 16, 400, 256),
+    # E4M3 pools in the page-major envelope, chunked-local layers, G = 5
+    "e4m3_envelope_chunked": ([(OT.CHUNKED, 64, 2), (OT.CHUNKED, 64, 2), (OT.FULL, 0, 2)], 10, 128,
+                              "e4m3", 16, 160, 64),
 }
+EXTRA = {"e4m3_envelope_chunked": dict(layout="envelope", k_scale=0.41, v_scale=1.7)}
 
 
 def _pair(name):
     layers, Hq, D, dt, ps, ring, _ = CASES[name]
     return Pair(layers, Hq=Hq, D=D, dtype=dt, ps=ps, size_full=ps * 256, size_swa=0, seed=7,
-                perm_free=True, max_reqs=6, max_ctx=ps * 64, ring_size=ring)
+                perm_free=True, max_reqs=6, max_ctx=ps * 64, ring_size=ring,
+                **EXTRA.get(name, {}))
 
 
 @pytest.mark.parametrize("name", list(CASES))
@@ -60,9 +67,11 @@ def test_ring_prefill_decode_evict_free(name):
     for step in range(6):
         P.evict(rows, lens, evicted, 3)
         seq = lens + 1
-        P.extend(rows, lens, seq)
+        # odd steps: the attention call stores the new token (swa_store_kv_attn_decode)
+        fused = step % 2 == 1
+        slots = P.extend(rows, lens, seq, store=not fused)
         P.check_state()
-        for l, (g, o) in P.decode_attention(rows, seq).items():
+        for l, (g, o) in P.decode_attention(rows, seq, new_slots=slots if fused else None).items():
             assert_close(g, o, tol, f"{name} decode step {step} layer {l}")
         lens = seq
     # Request 2 ends: full pages back, its ring slots unmapped.
