@@ -22,6 +22,7 @@ LAYER_FULL, LAYER_SLIDING, LAYER_CHUNKED = 0, 1, 2
 DTYPE_F32, DTYPE_BF16, DTYPE_E4M3 = 0, 1, 2
 LAYOUT_PER_LAYER, LAYOUT_ENVELOPE = 0, 1
 CTR_FULL_HEAD, CTR_FULL_COUNT, CTR_FULL_STAGED, CTR_SWA_HEAD, CTR_SWA_COUNT, CTR_SWA_STAGED, CTR_ERROR = range(7)
+SWA_DEVERR_WINDOW_EVICTED, SWA_DEVERR_COUNT, SWA_DEVERR_RANGE, SWA_DEVERR_TIMEOUT = 1, 2, 4, 8
 
 _STORE_TORCH = {DTYPE_F32: torch.float32, DTYPE_BF16: torch.bfloat16, DTYPE_E4M3: torch.uint8}
 

@@ -365,59 +365,67 @@ __global__ void k_release(const int64_t *idx, int64_t n, int do_full, int ps,
 }
 
 // -------------------------------------------------------------- eviction ---
-// Pass 1 (one CTA): per request the page-aligned range [old, new) and its
-// page count; offsets of each request's block in the freed run (later
-// requests ahead of earlier ones without need_sort: sequential prepends).
-__global__ void k_evict_plan(int bs, const int64_t *pre, const int64_t *evicted,
-                             const int64_t *prot, int lookback, int ps,
-                             int interval, int radix, EvictScratch sc,
-                             int64_t *counters, int max_pages, int need_sort,
-                             int32_t *err) {
-  for (int b = threadIdx.x; b < bs; b += blockDim.x) {
-    int64_t ev = evicted[b];
-    int64_t bound = pre[b] - (radix ? (lookback > ps ? lookback : ps) : lookback);
+// SWA page of request position t, or 0 when its mapping is not live (never
+// allocated, or already released by free_swa).
+__device__ inline int64_t live_swa_page(const int32_t *rt, int64_t row, int64_t t,
+                                        const int64_t *mapping, int64_t map_len, int ps) {
+  const int64_t f = rt[row + t];
+  const int64_t s = (f > 0 && f < map_len - 1) ? mapping[f] : 0;
+  return s > 0 ? s / ps : 0;
+}
+
+// Pass 1 (one CTA per request): the page-aligned range [old, new) and, for a
+// paged SWA pool, how many of its pages still hold a live SWA page (one
+// representative position per page: the range is page aligned and the ps
+// positions of one request page share one SWA page).  free_swa skips
+// positions whose mapping is not live, so only live pages are released; a
+// range with dead pages disagrees with the host's count (SWA_DEVERR_COUNT).
+__global__ void k_evict_plan(int bs, const int32_t *rt, int64_t rt_stride,
+                             const int64_t *req_idx, const int64_t *pre,
+                             const int64_t *evicted, const int64_t *prot, int lookback, int ps,
+                             int interval, int radix, const int64_t *mapping, int64_t map_len,
+                             bool count_live, EvictScratch sc, int32_t *err) {
+  __shared__ int64_t s_old, s_n;
+  const int b = blockIdx.x;
+  if (threadIdx.x == 0) {
+    const int64_t ev = evicted[b];
+    const int64_t bound = pre[b] - (radix ? (lookback > ps ? lookback : ps) : lookback);
     int64_t old_p = ev, new_p = ev, n = 0;
-    bool fire = !(interval > 0 && bound - ev < interval);
-    if (fire) {
+    if (!(interval > 0 && bound - ev < interval)) {
       new_p = bound > 0 ? (bound / ps) * ps : 0;
-      int64_t lo = ev > (prot ? prot[b] : 0) ? ev : (prot ? prot[b] : 0);
-      old_p = cdiv(lo, ps) * ps;
-      if (new_p > old_p) {
-        n = (new_p - old_p) / ps;
-        if (n > max_pages) {
-          set_error(err, SWA_DEVERR_SORT_CAP);
-          n = 0;
-          new_p = old_p;
-        }
-      } else {
-        new_p = old_p;
-      }
+      const int64_t pr = prot ? prot[b] : 0;
+      old_p = cdiv(ev > pr ? ev : pr, ps) * ps;
+      if (new_p > old_p) n = (new_p - old_p) / ps;
     }
     sc.old_pos[b] = old_p;
-    sc.new_pos[b] = (n > 0) ? new_p : -1;
+    sc.new_pos[b] = n > 0 ? new_p : -1;
     sc.npages[b] = n;
+    s_old = old_p;
+    s_n = count_live ? n : 0;
   }
   __syncthreads();
+  const int64_t n = s_n, old_p = s_old, row = req_idx[b] * rt_stride;
+  int64_t live = 0, unused = 0;
+  for (int64_t k = threadIdx.x; k < n; k += blockDim.x)
+    live += live_swa_page(rt, row, old_p + k * ps, mapping, map_len, ps) > 0;
+  block_sum2(live, unused);
   if (threadIdx.x == 0) {
-    int64_t acc = 0;
-    if (need_sort) {
-      for (int b = 0; b < bs; ++b) { sc.offset[b] = acc; acc += sc.npages[b]; }
-    } else {
-      for (int b = bs - 1; b >= 0; --b) { sc.offset[b] = acc; acc += sc.npages[b]; }
-    }
-    counters[8] = acc;
+    sc.nlive[b] = live;
+    if (live != n) set_error(err, SWA_DEVERR_COUNT);
   }
 }
 
-// Pass 2 (one CTA per request): the SWA page of every ps-th position of the
-// range (one representative per page: the range is page aligned and each
-// page holds ps consecutive positions), sorted ascending; mapping zeroed.
+// Pass 2 (one CTA per request): the live SWA pages of the range, ascending
+// (set bits of a bitmap over the pool's page ids in shared memory, then a
+// block-wide compaction), written at the request's place in the freed run -
+// later requests ahead of earlier ones without need_sort (sequential
+// prepends), in batch order into the staging list with need_sort - and the
+// range's mapping entries zeroed.
 __global__ void k_evict_apply(int bs, const int32_t *rt, int64_t rt_stride,
                               const int64_t *req_idx, int ps, PoolDev swa,
                               int64_t *mapping, int64_t map_len, EvictScratch sc,
-                              const int64_t *counters, int need_sort,
-                              int32_t *err) {
-  extern __shared__ int64_t keys[];
+                              int need_sort, int32_t *err) {
+  extern __shared__ uint32_t bm[];
   const int b = blockIdx.x;
   const int64_t n = sc.npages[b];
   if (n == 0) return;
@@ -430,60 +438,50 @@ __global__ void k_evict_apply(int bs, const int32_t *rt, int64_t rt_stride,
     }
     return;
   }
-  int64_t P2 = 1;
-  while (P2 < n) P2 <<= 1;
-  for (int64_t k = threadIdx.x; k < P2; k += blockDim.x) {
-    int64_t key = INT64_MAX;
-    if (k < n) {
-      int64_t f = rt[row + old_p + k * ps];
-      int64_t s = (f > 0 && f < map_len - 1) ? mapping[f] : 0;
-      if (s <= 0) {
-        set_error(err, SWA_DEVERR_COUNT);
-        key = 0;
-      } else {
-        key = s / ps;
-      }
-    }
-    keys[k] = key;
+  // This request's offset in the batch's freed run, and the run's length.
+  int64_t before = 0, total = 0;
+  for (int i = threadIdx.x; i < bs; i += blockDim.x) {
+    const int64_t v = sc.nlive[i];
+    total += v;
+    if (need_sort ? i < b : i > b) before += v;
+  }
+  block_sum2(before, total);
+  const int64_t words = (swa.cap + 1 + 31) / 32;
+  for (int64_t w = threadIdx.x; w < words; w += blockDim.x) bm[w] = 0;
+  __syncthreads();
+  for (int64_t k = threadIdx.x; k < n; k += blockDim.x) {
+    const int64_t page = live_swa_page(rt, row, old_p + k * ps, mapping, map_len, ps);
+    if (page > swa.cap) set_error(err, SWA_DEVERR_RANGE);
+    else if (page > 0) atomicOr(&bm[page >> 5], 1u << (page & 31));
   }
   __syncthreads();
-  // Bitonic sort, ascending.
-  for (int64_t size = 2; size <= P2; size <<= 1) {
-    for (int64_t stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int64_t i = threadIdx.x; i < P2; i += blockDim.x) {
-        int64_t j = i ^ stride;
-        if (j > i) {
-          bool up = (i & size) == 0;
-          int64_t a = keys[i], c = keys[j];
-          if ((a > c) == up) { keys[i] = c; keys[j] = a; }
-        }
-      }
-      __syncthreads();
-    }
+  if (need_sort) {
+    int64_t *st = swa.staged + *swa.nstaged + before;
+    compact_bitmap(bm, words, [&](int64_t j, int64_t page) { st[j] = page; });
+  } else {
+    const int64_t head = *swa.head, cap = swa.cap;
+    int64_t *ring = swa.ring;
+    compact_bitmap(bm, words, [&](int64_t j, int64_t page) {
+      ring[ring_pos(head, before + j - total, cap)] = page;
+    });
   }
+  __syncthreads();   // every mapping read above precedes the zeroing below
   for (int64_t t = old_p + threadIdx.x; t < new_p; t += blockDim.x) {
     int64_t f = rt[row + t];
     if (f > 0 && f < map_len - 1) mapping[f] = 0;
-  }
-  const int64_t total = counters[8];
-  const int64_t off = sc.offset[b];
-  if (need_sort) {
-    const int64_t ns = *swa.nstaged;
-    for (int64_t k = threadIdx.x; k < n; k += blockDim.x) swa.staged[ns + off + k] = keys[k];
-  } else {
-    const int64_t head = *swa.head;
-    for (int64_t k = threadIdx.x; k < n; k += blockDim.x)
-      swa.ring[ring_pos(head, off + k - total, swa.cap)] = keys[k];
   }
 }
 
 // Pass 3 (one CTA): move head / staged count, record the new evicted lengths.
 __global__ void k_evict_commit(int bs, int64_t *evicted, PoolDev swa,
-                               EvictScratch sc, int64_t *counters, int need_sort) {
-  for (int b = threadIdx.x; b < bs; b += blockDim.x)
+                               EvictScratch sc, int need_sort) {
+  int64_t total = 0, unused = 0;
+  for (int b = threadIdx.x; b < bs; b += blockDim.x) {
     if (sc.npages[b] > 0) evicted[b] = sc.new_pos[b];
+    total += sc.nlive[b];
+  }
+  block_sum2(total, unused);
   if (threadIdx.x == 0 && swa.ring_cost == 0) {
-    int64_t total = counters[8];
     if (need_sort) {
       *swa.nstaged += total;
     } else {
@@ -593,20 +591,18 @@ cudaError_t launch_release(Ctx &c, const int64_t *idx, int64_t n, bool do_full,
 
 cudaError_t launch_evict(Ctx &c, int bs, const int32_t *rt, int64_t rt_stride,
                          const int64_t *req_idx, const int64_t *pre, int64_t *evicted,
-                         const int64_t *prot, int interval, int radix, int max_pages_per_req,
-                         cudaStream_t s) {
+                         const int64_t *prot, int interval, int radix, cudaStream_t s) {
   if (bs == 0) return cudaSuccess;
-  k_evict_plan<<<1, 256, 0, s>>>(bs, pre, evicted, prot, c.lookback, c.cfg.page_size,
-                                  interval, radix, c.ev, c.counters, max_pages_per_req,
-                                  c.cfg.need_sort, c.err_word);
-  int64_t P2 = 1;
-  while (P2 < max_pages_per_req) P2 <<= 1;
-  size_t smem = (size_t)P2 * sizeof(int64_t);
+  const bool paged = c.swa.ring_cost == 0;
+  k_evict_plan<<<bs, 256, 0, s>>>(bs, rt, rt_stride, req_idx, pre, evicted, prot, c.lookback,
+                                  c.cfg.page_size, interval, radix, c.mapping, c.mapping_len,
+                                  paged, c.ev, c.err_word);
+  const size_t smem = paged ? bitmap_bytes(c.swa.cap) : 0;
   cudaFuncSetAttribute(k_evict_apply, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  k_evict_apply<<<bs, 512, smem, s>>>(bs, rt, rt_stride, req_idx, c.cfg.page_size, c.swa,
-                                       c.mapping, c.mapping_len, c.ev, c.counters,
-                                       c.cfg.need_sort, c.err_word);
-  k_evict_commit<<<1, 256, 0, s>>>(bs, evicted, c.swa, c.ev, c.counters, c.cfg.need_sort);
+  k_evict_apply<<<bs, 1024, smem, s>>>(bs, rt, rt_stride, req_idx, c.cfg.page_size, c.swa,
+                                       c.mapping, c.mapping_len, c.ev, c.cfg.need_sort,
+                                       c.err_word);
+  k_evict_commit<<<1, 256, 0, s>>>(bs, evicted, c.swa, c.ev, c.cfg.need_sort);
   return cudaGetLastError();
 }
 

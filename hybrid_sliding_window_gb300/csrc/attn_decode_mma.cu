@@ -10,7 +10,8 @@
 // CUDA-core FMAs cannot sustain at HBM speed, so the QK^T and PV products run
 // on tensor cores with the G query heads of one KV head as the M=16 rows of
 // mma.m16n8k16 (unused rows are zero).  Work item = (request, KV head, split
-// of up to 1024 keys); a CTA of 4 warps streams 64-key tiles through a
+// of 1024 to 4096 keys, a power of two chosen per launch from the longest
+// request); a CTA of 4 warps streams 64-key tiles through a
 // 3-stage cp.async pipeline (16-byte gathers of whole K/V rows, row address
 // from the index tables, out-of-range rows zero-filled without a read), each
 // warp owning 16 keys of every tile with its own online-softmax state in

@@ -33,8 +33,9 @@
 // their zero softmax weight cancels them exactly; page slots of a key tile
 // outside the range load an in-range page of the same request for the same
 // reason.
-// Every mbarrier wait has a poll limit; on expiry the kernel sets an error
-// bit, every role leaves its loop, and the TMEM is still released.
+// Every mbarrier wait has a poll limit; on expiry the kernel sets
+// SWA_DEVERR_TIMEOUT, every role leaves its loop, the TMA loads and tensor-core
+// products already issued are waited for, and the TMEM is released.
 #include <algorithm>
 
 #include <cuda_bf16.h>
@@ -122,6 +123,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
   *abort_flag = 1;
   return false;
+}
+// Bounded wait used only after an abort, for work that completes on its own
+// (issued TMA loads, committed tensor-core products): it ignores the flag.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  for (long i = 0; i < kSpinLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return;
+  }
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -242,7 +257,7 @@ constexpr int kOffK = 2 * kTileBytes;           // K stage 0, 1
 constexpr int kOffV = 4 * kTileBytes;           // V stage 0, 1
 constexpr int kOffRows = 6 * kTileBytes;        // int32 page rows [max_pages]
 enum { B_FULLK = 0, B_EMPTYK = 2, B_FULLV = 4, B_EMPTYV = 6, B_SDONE = 8, B_PREADY = 10,
-       B_ODONE = 12, B_COUNT = 13 };
+       B_ODONE = 12, B_DRAIN = 13, B_COUNT = 14 };
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_extend_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -280,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_PREADY + i), kRows);
     }
     mbar_init(bar(B_ODONE), 1);
+    mbar_init(bar(B_DRAIN), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
@@ -293,6 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // of its earlier items) or item count n_done, so the rings run on across
   // items; each item ends with all roles joined (its Q tiles and TMEM free).
   int tg0 = 0, n_done = 0;
+  // Producer only: phases armed so far on each K / V "full" barrier, so that
+  // an abort can wait for the loads still in flight.
+  int armK[2] = {0, 0}, armV[2] = {0, 0};
   for (int item = blockIdx.x; item < P.items_upper; item += gridDim.x) {
   __syncthreads();   // every thread has read the previous item's fields
   // ---- work item: two Q tiles of one request, latest first ----
@@ -387,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           const uint32_t full = bar((kv ? B_FULLV : B_FULLK) + s);
           mbar_expect_tx(full, (uint32_t)kTileBytes);   // every page slot is loaded
+          ++(kv ? armV : armK)[s];
           const uint32_t dst = sb + (kv ? kOffV : kOffK) + s * kTileBytes;
           for (int i = 0; i < pages_per_tile; ++i) {
             const int pi = t * pages_per_tile + i;
@@ -644,7 +664,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (s_abort) break;
   tc_fence_after();
   }
-  if (s_abort && tid == 0) set_error(P.err, SWA_DEVERR_RANGE);
+  if (s_abort) {
+    // A role gave up a wait.  Loads and products already issued complete on
+    // their own; wait for them before the shared memory and TMEM they write
+    // are released.
+    if (tid == 0) set_error(P.err, SWA_DEVERR_TIMEOUT);
+    if (warp == 9 && lane == 0) {
+      for (int i = 0; i < 2; ++i) {
+        if (armK[i]) mbar_drain(bar(B_FULLK + i), (armK[i] - 1) & 1);
+        if (armV[i]) mbar_drain(bar(B_FULLV + i), (armV[i] - 1) & 1);
+      }
+    }
+    if (warp == 8 && lane == 0) {
+      tc_commit(bar(B_DRAIN));   // tracks every product this thread issued
+      mbar_drain(bar(B_DRAIN), 0);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {

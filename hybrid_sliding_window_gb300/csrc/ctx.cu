@@ -22,7 +22,6 @@ namespace {
 using swa::Ctx;
 
 thread_local std::string g_create_err;
-constexpr int kEvictMaxPages = 8192;   // pages one request may return per pass
 constexpr int64_t kMaxBitmapPages = 1700000;  // bitmap of a pool fits in shared memory
 
 swa_status fail(swa_ctx *c, swa_status st, const std::string &msg) {
@@ -197,6 +196,10 @@ void swa::set_ctx_error(swa_ctx *ctx, const char *msg) {
   if (ctx) ctx->err = msg;
 }
 
+size_t swa::decode_ws_zero_bytes(const swa_ctx *ctx, int64_t bs) {
+  return ctx ? swa::ws_partials_off(*ctx, bs) : 0;
+}
+
 extern "C" {
 
 swa_status swa_pool_sizes(int64_t mem_bytes, int64_t F, int64_t S, int32_t L_full,
@@ -255,6 +258,7 @@ size_t swa_state_bytes(const swa_config *cfg) {
 
 swa_status swa_ctx_create(const swa_config *cfg, void *state_dev, const int64_t *init_free_full,
                           const int64_t *init_free_swa, swa_stream_t stream, swa_ctx **out) {
+  SWA_NVTX("swa_ctx_create");
   if (!out || !state_dev) return fail(nullptr, SWA_ERR_INVALID, "null state or output pointer");
   *out = nullptr;
   if (reinterpret_cast<uintptr_t>(state_dev) % 256)
@@ -345,6 +349,7 @@ int64_t swa_available_size(const swa_ctx *c) {
 }
 
 swa_status swa_device_check(swa_ctx *c, swa_stream_t stream, int32_t *err) {
+  SWA_NVTX("swa_device_check");
   if (!c) return SWA_ERR_INVALID;
   CUDA_TRY(c, cudaStreamSynchronize((cudaStream_t)stream));
   int32_t w = 0;
@@ -356,6 +361,7 @@ swa_status swa_device_check(swa_ctx *c, swa_stream_t stream, int32_t *err) {
 }
 
 swa_status swa_sync_counts(swa_ctx *c, swa_stream_t stream) {
+  SWA_NVTX("swa_sync_counts");
   if (!c) return SWA_ERR_INVALID;
   CUDA_TRY(c, cudaStreamSynchronize((cudaStream_t)stream));
   int64_t h[8];
@@ -371,6 +377,7 @@ swa_status swa_sync_counts(swa_ctx *c, swa_stream_t stream) {
 // -------------------------------------------------------------- allocation ---
 swa_status swa_alloc(swa_ctx *c, int64_t need, int64_t *out_full, int64_t *out_swa,
                      swa_stream_t stream) {
+  SWA_NVTX("swa_alloc");
   if (!c || need < 0 || (need > 0 && !out_full)) return fail(c, SWA_ERR_INVALID, "bad alloc args");
   if (need % c->cfg.page_size) return fail(c, SWA_ERR_INVALID, "need_size is not page aligned");
   if (c->ring_cost) return fail(c, SWA_ERR_INVALID, "plain alloc has no request slot in ring mode");
@@ -427,6 +434,7 @@ swa_status swa_alloc_extend(swa_ctx *c, int32_t bs, const int64_t *prefix_lens,
                             const int64_t *prefix_lens_host, const int64_t *seq_lens_host,
                             int64_t *out_full, int64_t *out_swa, int32_t *req_to_token,
                             int64_t rt_stride, const int64_t *req_idx, swa_stream_t stream) {
+  SWA_NVTX("swa_alloc_extend");
   if (c && bs > 0 && (!prefix_lens || !prefix_lens_host))
     return fail(c, SWA_ERR_INVALID, "null prefix lengths");
   return alloc_common(c, bs, prefix_lens, seq_lens, last_loc, prefix_lens_host, seq_lens_host,
@@ -437,6 +445,7 @@ swa_status swa_alloc_decode(swa_ctx *c, int32_t bs, const int64_t *seq_lens,
                             const int64_t *last_loc, const int64_t *seq_lens_host,
                             int64_t *out_full, int64_t *out_swa, int32_t *req_to_token,
                             int64_t rt_stride, const int64_t *req_idx, swa_stream_t stream) {
+  SWA_NVTX("swa_alloc_decode");
   if (c && seq_lens_host)
     for (int b = 0; b < bs; ++b)
       if (seq_lens_host[b] < 1) return fail(c, SWA_ERR_INVALID, "decode seq_lens must be >= 1");
@@ -447,6 +456,7 @@ swa_status swa_alloc_decode(swa_ctx *c, int32_t bs, const int64_t *seq_lens,
 swa_status swa_translate_for_kernel(swa_ctx *c, const int64_t *v2p, int64_t n_pages,
                                     const int64_t *virt, int64_t n, int32_t page_size,
                                     int32_t multiplier, int64_t *out, swa_stream_t stream) {
+  SWA_NVTX("swa_translate_for_kernel");
   if (n < 0 || n_pages < 0 || page_size < 1 || multiplier < 1 ||
       (n > 0 && (!v2p || !virt || !out)))
     return fail(c, SWA_ERR_INVALID, "bad translate_for_kernel args");
@@ -458,6 +468,7 @@ swa_status swa_translate_for_kernel(swa_ctx *c, const int64_t *v2p, int64_t n_pa
 
 swa_status swa_translate(swa_ctx *c, const int64_t *full_loc, int64_t n, int64_t *swa_loc,
                          swa_stream_t stream) {
+  SWA_NVTX("swa_translate");
   if (!c || n < 0 || (n > 0 && (!full_loc || !swa_loc))) return fail(c, SWA_ERR_INVALID, "bad translate args");
   CUDA_TRY(c, swa::launch_translate(*c, full_loc, n, swa_loc, (cudaStream_t)stream));
   return SWA_OK;
@@ -466,6 +477,7 @@ swa_status swa_translate(swa_ctx *c, const int64_t *full_loc, int64_t n, int64_t
 // ----------------------------------------------------------------- release ---
 swa_status swa_free(swa_ctx *c, const int64_t *full_idx, int64_t n, int64_t n_full_pages,
                     int64_t n_swa_pages, swa_stream_t stream) {
+  SWA_NVTX("swa_free");
   if (!c || n < 0 || (n > 0 && !full_idx)) return fail(c, SWA_ERR_INVALID, "bad free args");
   if (n == 0) return SWA_OK;
   CUDA_TRY(c, swa::launch_release(*c, full_idx, n, true, n_full_pages, n_swa_pages,
@@ -477,6 +489,7 @@ swa_status swa_free(swa_ctx *c, const int64_t *full_idx, int64_t n, int64_t n_fu
 
 swa_status swa_free_swa(swa_ctx *c, const int64_t *full_idx, int64_t n, int64_t n_swa_pages,
                         swa_stream_t stream) {
+  SWA_NVTX("swa_free_swa");
   if (!c || n < 0 || (n > 0 && !full_idx)) return fail(c, SWA_ERR_INVALID, "bad free_swa args");
   if (n == 0) return SWA_OK;
   CUDA_TRY(c, swa::launch_release(*c, full_idx, n, false, -1, n_swa_pages, (cudaStream_t)stream));
@@ -489,6 +502,7 @@ swa_status swa_evict_swa(swa_ctx *c, int32_t bs, const int32_t *rt, int64_t rt_s
                          const int64_t *protected_lens, const int64_t *pre_h,
                          int64_t *evicted_h, const int64_t *protected_h, int32_t interval,
                          int32_t radix, swa_stream_t stream) {
+  SWA_NVTX("swa_evict_swa");
   if (!c) return SWA_ERR_INVALID;
   if (bs < 0 || bs > c->cfg.max_batch) return fail(c, SWA_ERR_INVALID, "bs out of range");
   if (bs == 0) return SWA_OK;
@@ -507,8 +521,6 @@ swa_status swa_evict_swa(swa_ctx *c, int32_t bs, const int32_t *rt, int64_t rt_s
     const int64_t old = cdiv(std::max(ev, prot), ps) * ps;
     if (nw > old) {
       const int64_t n = (nw - old) / ps;
-      if (n > kEvictMaxPages)
-        return fail(c, SWA_ERR_INVALID, "eviction range longer than 8192 pages; evict more often");
       if (nw > rt_stride) return fail(c, SWA_ERR_INVALID, "eviction range beyond req_to_token row");
       total += n;
       new_ev[b] = nw;
@@ -519,8 +531,7 @@ swa_status swa_evict_swa(swa_ctx *c, int32_t bs, const int32_t *rt, int64_t rt_s
   // steps between interval triggers) launches nothing.
   if (total > 0)
     CUDA_TRY(c, swa::launch_evict(*c, bs, rt, rt_stride, req_idx, pre_lens, evicted,
-                                  protected_lens, interval, radix, kEvictMaxPages,
-                                  (cudaStream_t)stream));
+                                  protected_lens, interval, radix, (cudaStream_t)stream));
   if (!c->ring_cost) mirror_release(c, false, total);
   std::copy(new_ev.begin(), new_ev.end(), evicted_h);
   return SWA_OK;
@@ -530,6 +541,7 @@ swa_status swa_evict_swa(swa_ctx *c, int32_t bs, const int32_t *rt, int64_t rt_s
 swa_status swa_store_kv(swa_ctx *c, int32_t layer, const void *k, const void *v, int64_t n,
                         const int64_t *full_loc, const int64_t *swa_loc, float k_scale,
                         float v_scale, swa_stream_t stream) {
+  SWA_NVTX("swa_store_kv");
   if (!c) return SWA_ERR_INVALID;
   if (layer < 0 || layer >= c->cfg.num_layers) return fail(c, SWA_ERR_INVALID, "layer out of range");
   if (n < 0 || (n > 0 && (!k || !v || !full_loc))) return fail(c, SWA_ERR_INVALID, "bad store args");
@@ -550,6 +562,7 @@ size_t swa_plan_bytes(const swa_ctx *c, int32_t bs, int32_t max_new) {
 swa_status swa_plan(swa_ctx *c, int32_t bs, const int32_t *rt, int64_t rt_stride,
                     const int64_t *req_idx, const int64_t *prefix_lens, const int64_t *seq_lens,
                     int32_t max_new, void *plan, size_t plan_bytes, swa_stream_t stream) {
+  SWA_NVTX("swa_plan");
   if (!c) return SWA_ERR_INVALID;
   if (bs < 0 || bs > c->cfg.max_batch) return fail(c, SWA_ERR_INVALID, "bs out of range");
   if (bs == 0) return SWA_OK;
@@ -562,19 +575,15 @@ swa_status swa_plan(swa_ctx *c, int32_t bs, const int32_t *rt, int64_t rt_stride
 }
 
 // --------------------------------------------------------------- attention ---
-static bool use_tma(const swa_ctx *c, int layer) {
-  return c->forced_path == 3 && swa::tma_decode_supported(*c, layer);
-}
 static bool use_mma(const swa_ctx *c, int layer) {
   return c->forced_path != 0 && swa::mma_decode_supported(*c, layer);
 }
 static bool use_tc(const swa_ctx *c, int layer) {
-  return (c->forced_path == -1 || c->forced_path == 3) && swa::tc_extend_supported(*c, layer);
+  return c->forced_path == -1 && swa::tc_extend_supported(*c, layer);
 }
 
 size_t swa_attn_decode_ws_bytes(const swa_ctx *c, int32_t layer, int32_t bs, int32_t max_seq_len) {
   if (!c || layer < 0 || layer >= c->cfg.num_layers || bs < 0 || max_seq_len < 1) return 0;
-  if (use_tma(c, layer)) return swa::tma_decode_ws_bytes(*c, layer, bs, max_seq_len);
   if (use_mma(c, layer)) return swa::mma_decode_ws_bytes(*c, layer, bs, max_seq_len);
   return swa::simt_ws_bytes(*c, layer, bs, max_seq_len);
 }
@@ -625,7 +634,7 @@ static swa_status attn_decode_impl(swa_ctx *c, int32_t layer, int32_t bs, const 
   a.ws = ws;
   a.ws_bytes = ws_bytes;
   cudaStream_t s = (cudaStream_t)stream;
-  const bool mma = !use_tma(c, layer) && use_mma(c, layer);
+  const bool mma = use_mma(c, layer);
   if (store && mma) {
     a.k_new = k_new;
     a.v_new = v_new;
@@ -634,10 +643,7 @@ static swa_status attn_decode_impl(swa_ctx *c, int32_t layer, int32_t bs, const 
   } else if (store) {
     CUDA_TRY(c, swa::launch_store(*c, layer, k_new, v_new, bs, full_loc, swa_loc, k_scale, v_scale, s));
   }
-  if (use_tma(c, layer)) {
-    c->last_path = 3;
-    CUDA_TRY(c, swa::launch_attn_decode_tma(*c, a, s));
-  } else if (mma) {
+  if (mma) {
     c->last_path = 1;
     CUDA_TRY(c, swa::launch_attn_decode_mma(*c, a, s));
   } else {
@@ -652,6 +658,7 @@ swa_status swa_attn_decode(swa_ctx *c, int32_t layer, int32_t bs, const int32_t 
                            int32_t max_seq_len, const void *plan, const void *q,
                            const float *sinks, float sm_scale, float k_scale, float v_scale,
                            void *out, void *ws, size_t ws_bytes, swa_stream_t stream) {
+  SWA_NVTX("swa_attn_decode");
   return attn_decode_impl(c, layer, bs, rt, rt_stride, req_idx, seq_lens, max_seq_len, plan, q,
                           nullptr, nullptr, nullptr, nullptr, sinks, sm_scale, k_scale, v_scale,
                           out, ws, ws_bytes, stream);
@@ -665,6 +672,7 @@ swa_status swa_store_kv_attn_decode(swa_ctx *c, int32_t layer, int32_t bs, const
                                     const float *sinks, float sm_scale, float k_scale,
                                     float v_scale, void *out, void *ws, size_t ws_bytes,
                                     swa_stream_t stream) {
+  SWA_NVTX("swa_store_kv_attn_decode");
   if (c && bs > 0 && (!k_new || !v_new || !full_loc)) return fail(c, SWA_ERR_INVALID, "bad store args");
   return attn_decode_impl(c, layer, bs, rt, rt_stride, req_idx, seq_lens, max_seq_len, plan, q,
                           k_new, v_new, full_loc, swa_loc, sinks, sm_scale, k_scale, v_scale, out,
@@ -684,6 +692,7 @@ swa_status swa_attn_extend(swa_ctx *c, int32_t layer, int32_t bs, const int32_t 
                            int32_t max_new, int32_t max_seq_len, const void *plan, const void *q,
                            const float *sinks, float sm_scale, float k_scale, float v_scale,
                            void *out, void *ws, size_t ws_bytes, swa_stream_t stream) {
+  SWA_NVTX("swa_attn_extend");
   if (!c) return SWA_ERR_INVALID;
   if (layer < 0 || layer >= c->cfg.num_layers) return fail(c, SWA_ERR_INVALID, "layer out of range");
   if (bs < 0 || bs > c->cfg.max_batch || n_tokens < 0) return fail(c, SWA_ERR_INVALID, "bs out of range");
@@ -732,7 +741,7 @@ int32_t swa_last_attn_path(const swa_ctx *c) { return c ? c->last_path : -1; }
 
 swa_status swa_set_attn_path(swa_ctx *c, int32_t path) {
   if (!c) return SWA_ERR_INVALID;
-  if (path < -1 || path > 3 || path == 2) return fail(c, SWA_ERR_INVALID, "path must be -1, 0, 1 or 3");
+  if (path < -1 || path > 1) return fail(c, SWA_ERR_INVALID, "path must be -1, 0 or 1");
   c->forced_path = path;
   return SWA_OK;
 }

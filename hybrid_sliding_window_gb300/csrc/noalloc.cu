@@ -12,41 +12,31 @@
 // The array is kNoAllocScratchBytes (32 MiB) of device memory that every GPU
 // loading this library keeps until the process exits.  Every call on a
 // device shares it and it keeps the last call's contents, so each call
-// clears the bytes it needs first, and calls that overlap on the GPU (for
-// example on two streams) race on it.
+// clears the part that must start at zero (the work counters and merge
+// tickets; the kernels write every partial before they read it), and calls
+// that overlap on the GPU (for example on two streams) race on it.
 #include <cuda_runtime.h>
 #include <stdint.h>
-
-#include <mutex>
 
 #include "swa_internal.h"
 
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
 
-std::mutex g_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
-
 // Device address of g_decode_scratch on the current device.  In host code the
-// array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+// array's name is only a host-side stand-in, never a device address.  The
+// lookup is a host-side query that allocates nothing; it runs on every call,
+// so no address outlives the context it came from (after cudaDeviceReset the
+// module is loaded again and the array gets a new address).  The first call
+// on a device loads the module there.
 cudaError_t scratch_address(void **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void *p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return cudaSuccess;
 }
 
@@ -61,6 +51,7 @@ extern "C" swa_status swa_attn_decode_noalloc(swa_ctx *ctx, int32_t layer, int32
                                               const void *q, const float *sinks, float sm_scale,
                                               float k_scale, float v_scale, void *out,
                                               swa_stream_t stream) {
+  SWA_NVTX("swa_attn_decode_noalloc");
   if (!ctx) return SWA_ERR_INVALID;
   if (bs == 0) return SWA_OK;
   const size_t need = swa_attn_decode_ws_bytes(ctx, layer, bs, max_seq_len);
@@ -80,7 +71,8 @@ extern "C" swa_status swa_attn_decode_noalloc(swa_ctx *ctx, int32_t layer, int32
     swa::set_ctx_error(ctx, cudaGetErrorString(e));
     return SWA_ERR_CUDA;
   }
-  e = cudaMemsetAsync(scratch, 0, need, (cudaStream_t)stream);
+  const size_t zero = swa::decode_ws_zero_bytes(ctx, bs);
+  e = cudaMemsetAsync(scratch, 0, zero < need ? zero : need, (cudaStream_t)stream);
   if (e != cudaSuccess) {
     swa::set_ctx_error(ctx, cudaGetErrorString(e));
     return SWA_ERR_CUDA;

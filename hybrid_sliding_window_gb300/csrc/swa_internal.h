@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include <string>
@@ -13,6 +14,16 @@
 namespace swa {
 
 constexpr int kMaxHeadDim = 256;
+
+// One NVTX range per C-ABI call, named after the entry point, so a profiler
+// timeline groups each call's launches (a no-op unless a tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange &) = delete;
+  NvtxRange &operator=(const NvtxRange &) = delete;
+};
+#define SWA_NVTX(name) ::swa::NvtxRange swa_nvtx_range_(name)
 
 // One free-page ledger on the device: a ring of page ids (front at head),
 // a staging list (need_sort) and three counters in the state blob.
@@ -59,8 +70,8 @@ struct LayerInfo {
 struct EvictScratch {
   int64_t *old_pos;
   int64_t *new_pos;
-  int64_t *npages;
-  int64_t *offset;
+  int64_t *npages;   // pages of the range [old, new)
+  int64_t *nlive;    // of those, pages that still hold a live SWA page
 };
 
 // Plan workspace layout: header int32 [bs][4] = {lo, hi, first_page, n_pages},
@@ -109,6 +120,9 @@ inline size_t ws_tickets_bytes(const Ctx &c, int64_t nq) {
   return ((size_t)n * hmax * sizeof(int32_t) + 255) / 256 * 256;
 }
 inline size_t ws_partials_off(const Ctx &c, int64_t nq) { return 256 + ws_tickets_bytes(c, nq); }
+// Leading bytes of a decode workspace that must be zero before a launch (the
+// counters and tickets; the kernels write every partial before reading it).
+size_t decode_ws_zero_bytes(const swa_ctx *ctx, int64_t bs);
 
 // ---- launchers (alloc.cu) -------------------------------------------------
 cudaError_t launch_init_state(Ctx &c, const int64_t *init_full,
@@ -128,7 +142,7 @@ cudaError_t launch_release(Ctx &c, const int64_t *idx, int64_t n, bool do_full,
 cudaError_t launch_evict(Ctx &c, int bs, const int32_t *rt, int64_t rt_stride,
                          const int64_t *req_idx, const int64_t *pre,
                          int64_t *evicted, const int64_t *prot, int interval,
-                         int radix, int max_pages_per_req, cudaStream_t s);
+                         int radix, cudaStream_t s);
 cudaError_t launch_translate(Ctx &c, const int64_t *full_loc, int64_t n,
                              int64_t *swa_loc, cudaStream_t s);
 cudaError_t launch_translate_for_kernel(const int64_t *v2p, int64_t n_pages,
@@ -183,10 +197,6 @@ cudaError_t launch_attn_simt(Ctx &c, const AttnArgs &a, cudaStream_t s);
 bool mma_decode_supported(const Ctx &c, int layer);
 size_t mma_decode_ws_bytes(const Ctx &c, int layer, int64_t nq, int max_seq_len);
 cudaError_t launch_attn_decode_mma(Ctx &c, const AttnArgs &a, cudaStream_t s);
-
-bool tma_decode_supported(const Ctx &c, int layer);
-size_t tma_decode_ws_bytes(const Ctx &c, int layer, int64_t nq, int max_seq_len);
-cudaError_t launch_attn_decode_tma(Ctx &c, const AttnArgs &a, cudaStream_t s);
 
 bool tc_extend_supported(const Ctx &c, int layer);
 // Builds the TMA tensor maps of one layer (bf16, D = 128, per-layer layout);

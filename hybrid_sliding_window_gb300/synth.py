@@ -85,6 +85,16 @@ def tokens(seed: int, stream: int, layer: int, reqs, positions, heads: int,
     return to_bf16_values(x) if bf16 else x
 
 
+def tokens_head(seed: int, stream: int, layer: int, req: int, positions, head: int,
+                dim: int, bf16: bool = True) -> np.ndarray:
+    """Values ``[n, dim]`` of one head for tokens ``(req, positions[i])``:
+    the ``head`` slice of ``tokens`` without drawing the other heads."""
+    pos = np.asarray(positions, dtype=np.int64).reshape(-1, 1)
+    d = np.arange(dim, dtype=np.int64).reshape(1, -1)
+    x = normal_f32(seed, stream, element_index(layer, req, pos, head, d))
+    return to_bf16_values(x) if bf16 else x
+
+
 def sinks(seed: int, layer: int, num_q_heads: int) -> np.ndarray:
     """Per-head sink logits ``[Hq]`` of one layer (float32)."""
     return tokens(seed, STREAM_SINK, layer, [0], [0], num_q_heads, 1,

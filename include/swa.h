@@ -84,7 +84,8 @@ enum swa_device_error {
   SWA_DEVERR_WINDOW_EVICTED = 1,  /* an attended key's SWA mapping was 0        */
   SWA_DEVERR_COUNT = 2,           /* freed page count differs from host count  */
   SWA_DEVERR_RANGE = 4,           /* slot / page / position out of range       */
-  SWA_DEVERR_SORT_CAP = 8         /* an eviction range exceeded the sort size  */
+  SWA_DEVERR_TIMEOUT = 8          /* a kernel gave up a bounded wait (its
+                                     outputs for the launch are incomplete)    */
 };
 
 typedef struct swa_layer {
@@ -486,12 +487,15 @@ swa_status swa_store_kv_attn_decode(swa_ctx *ctx, int32_t layer, int32_t bs,
  * (swa_attn_decode_noalloc_max_bytes()), which every GPU that loads the
  * library holds until the process exits.  A batch whose scratch
  * (swa_attn_decode_ws_bytes) exceeds it is rejected with SWA_ERR_INVALID and
- * a message.  The call allocates nothing: it clears the scratch bytes it
- * needs (cudaMemsetAsync on `stream`) and runs the same kernels.  The first
- * call on a device looks up the array's device address, so make that first
- * call before any stream capture.  All calls on a device share the array and
- * it keeps the last call's contents; calls that overlap on the GPU (e.g. on
- * different streams) race on it. */
+ * a message.  The call allocates nothing: it looks up the array's device
+ * address (a host-side query, on every call, so no address outlives a
+ * cudaDeviceReset), clears the array's counters and merge tickets
+ * (cudaMemsetAsync on `stream`; the partial results are not cleared - the
+ * kernels write each one before reading it) and runs the same kernels as
+ * swa_attn_decode.  The first call on a device loads the array onto that
+ * device, so make that first call before any stream capture.  All calls on a
+ * device share the array and it keeps the last call's contents; calls that
+ * overlap on the GPU (e.g. on different streams) race on it. */
 size_t swa_attn_decode_noalloc_max_bytes(void);
 swa_status swa_attn_decode_noalloc(swa_ctx *ctx, int32_t layer, int32_t bs,
                                    const int32_t *req_to_token,
@@ -520,15 +524,12 @@ swa_status swa_attn_extend(swa_ctx *ctx, int32_t layer, int32_t bs,
 
 /* Which kernel family the last attention call on ctx launched
  * (0 = generic CUDA-core kernel, 1 = tensor-core decode fed by cp.async,
- * 2 = tcgen05 extend, 3 = persistent TMA-fed tensor-core decode), for tests
- * and profiling. */
+ * 2 = tcgen05 extend), for tests and profiling. */
 int32_t swa_last_attn_path(const swa_ctx *ctx);
 /* Restricts the kernel family attention calls on ctx may take: -1 = best
  * available (default: cp.async tensor-core decode, tcgen05 extend), 0 =
  * generic CUDA-core kernel only, 1 = cp.async tensor-core decode and no
- * tcgen05 extend, 3 = the persistent TMA-fed decode where it applies (an
- * alternative decode kernel, slower than the default on the measured
- * workloads).  Any other value is SWA_ERR_INVALID.  For tests and
+ * tcgen05 extend.  Any other value is SWA_ERR_INVALID.  For tests and
  * profiling. */
 swa_status swa_set_attn_path(swa_ctx *ctx, int32_t path);
 

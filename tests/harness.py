@@ -87,6 +87,15 @@ class Pair:
         self.sinks = [synth.sinks(seed, l, Hq) for l in range(len(layers))]
         self.sinks_d = [torch.tensor(s, device=dev) for s in self.sinks]
         self.scale = 1.0 / np.sqrt(D)
+        # Optional input shaping for wide score ranges: q is multiplied by
+        # q_gain, the K rows of position t by k_gain(t); the products are
+        # rounded to the input dtype, so both sides read the same values.
+        self.q_gain = 1.0
+        self.k_gain = None
+
+    def set_sinks(self, l, values):
+        self.sinks[l] = np.asarray(values, np.float32)
+        self.sinks_d[l] = torch.tensor(self.sinks[l], device="cuda")
 
     # ------------------------------------------------------------- inputs ---
     def kv_in(self, l, reqs, pos):
@@ -94,11 +103,19 @@ class Pair:
         bf = self.dtype != "f32"
         k = synth.tokens(self.seed, synth.STREAM_K, l, reqs, pos, hkv, self.D, bf16=bf)
         v = synth.tokens(self.seed, synth.STREAM_V, l, reqs, pos, hkv, self.D, bf16=bf)
+        if self.k_gain is not None:
+            g = np.asarray(self.k_gain(np.asarray(pos, np.int64)), np.float32).reshape(-1, 1, 1)
+            k = (k * g).astype(np.float32)
+            k = synth.to_bf16_values(k) if bf else k
         return k, v
 
     def q_in(self, l, reqs, pos):
         bf = self.dtype != "f32"
-        return synth.tokens(self.seed, synth.STREAM_Q, l, reqs, pos, self.Hq, self.D, bf16=bf)
+        q = synth.tokens(self.seed, synth.STREAM_Q, l, reqs, pos, self.Hq, self.D, bf16=bf)
+        if self.q_gain != 1.0:
+            q = (q * np.float32(self.q_gain)).astype(np.float32)
+            q = synth.to_bf16_values(q) if bf else q
+        return q
 
     def to_dev(self, x):
         t = torch.tensor(x, device="cuda")

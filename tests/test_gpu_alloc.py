@@ -123,6 +123,53 @@ def test_random_sequences_match_oracle(ps, need_sort):
     P.oa.check_no_duplicate_pages()
 
 
+@pytest.mark.parametrize("need_sort", [False, True])
+def test_evict_over_partly_freed_range(need_sort):
+    """free_swa of page-aligned parts of two requests, then an eviction pass
+    whose ranges cover them ([SWA note], "runtime": free_swa skips tokens
+    whose mapping is already 0).  Only the pages still live are released, in
+    the oracle's order, no page 0 enters a free list, and the eviction flags
+    that its page count differs from the host's (the host counted the whole
+    range) until the mirrors are reloaded."""
+    P = _pair(4, need_sort=need_sort, nf=64, ns=40)
+    P.extend([1, 2], [0, 0], [40, 33])
+    _free_gpu(P, [int(x) for x in P.ort[1, 8:20]], swa_only=True)
+    _free_gpu(P, [int(x) for x in P.ort[2, 4:8]], swa_only=True)
+    P.check_state()
+    ev = np.zeros(2, np.int64)
+    P.evict([1, 2], [40, 33], ev, 0)          # ranges [0, 32) and [0, 24)
+    assert ev.tolist() == [32, 24]
+    torch.cuda.synchronize()
+    assert api.swa_device_check(P.ctx) == api.SWA_DEVERR_COUNT
+    api.swa_sync_counts(P.ctx)
+    P.check_state()
+    free, staged = P.ctx.free_list(False)
+    assert 0 not in free + staged
+    assert len(set(free + staged)) == len(free + staged)
+    P.oa.check_no_duplicate_pages()
+
+
+@pytest.mark.parametrize("need_sort", [False, True])
+def test_evict_twenty_thousand_slots_in_one_pass(need_sort):
+    """One request's out-of-window range of 20 193 tokens at page size 1 is
+    released by one eviction call ([SWA note], "runtime":
+    free_swa_out_of_window_slots takes the whole range), bit exact against the
+    oracle; a second request evicts a short range in the same pass."""
+    P = Pair(LAYERS, Hq=2, D=32, dtype="f32", ps=1, size_full=24000, size_swa=22000,
+             need_sort=need_sort, perm_free=True, seed=5, max_ctx=20300, max_reqs=3)
+    lens = np.zeros(2, np.int64)
+    for stop in (6000, 12000, 18000, 20200):
+        new = np.array([stop, min(stop // 20, 900)], np.int64)
+        P.extend([1, 2], lens, new)
+        lens = new
+    P.check_state()
+    ev = np.zeros(2, np.int64)
+    P.evict([1, 2], lens, ev, 0)
+    assert ev.tolist() == [20200 - 7, 900 - 7]
+    P.check_state()
+    P.oa.check_no_duplicate_pages()
+
+
 def test_free_without_counts_marks_mirror_stale_until_sync():
     P = _pair(4)
     P.extend([1, 2], [0, 0], [9, 13])

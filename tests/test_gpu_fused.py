@@ -60,7 +60,7 @@ SPEC_CASES = {
 }
 
 
-@pytest.mark.parametrize("path", [-1, 3, 0], ids=["mma", "tma", "generic"])
+@pytest.mark.parametrize("path", [-1, 0], ids=["mma", "generic"])
 @pytest.mark.parametrize("case", list(SPEC_CASES))
 def test_fused_equals_two_calls(case, path):
     spec = SPEC_CASES[case]

@@ -45,8 +45,7 @@ def small(name, **kw):
     return dataclasses.replace(SPECS[name], **kw)
 
 
-PATHS = [pytest.param(-1, 1, id="default-cp.async-mma"), pytest.param(3, 3, id="tma-persistent"),
-         pytest.param(0, 0, id="generic")]
+PATHS = [pytest.param(-1, 1, id="default-cp.async-mma"), pytest.param(0, 0, id="generic")]
 
 
 @pytest.mark.parametrize("path,expect", PATHS)
