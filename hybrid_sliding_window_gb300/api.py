@@ -110,6 +110,18 @@ SIGNATURES = {
     "swa_last_attn_path": (I32, [P]),
     "swa_set_attn_path": (I32, [P, I32]),
     "swa_synth_tokens": (I32, [C.c_uint64, I32, I32, P, P, I64, I32, I32, I32, P, P]),
+    "swa_unified_state_bytes": (SZ, [I64, I32]),
+    "swa_unified_create": (I32, [I64, I32, I32, P, P, P]),
+    "swa_unified_destroy": (None, [P]),
+    "swa_unified_last_error": (C.c_char_p, [P]),
+    "swa_unified_state_pointers": (I32, [P, P]),
+    "swa_unified_available_size": (I64, [P]),
+    "swa_unified_sync": (I32, [P, P]),
+    "swa_unified_device_check": (I32, [P, P, P]),
+    "swa_unified_alloc_extend": (I32, [P, I32, P, P, P, P, P, P, P, I64, P, P]),
+    "swa_unified_free_swa": (I32, [P, P, I64, P]),
+    "swa_unified_free": (I32, [P, P, I64, P]),
+    "swa_unified_evict_swa": (I32, [P, I32, I32, P, I64, P, P, P, P, P, P, P, I32, I32, P]),
 }
 
 _lib = None
@@ -522,3 +534,129 @@ def swa_synth_tokens(seed, stream_id, layer, req, pos, heads, dim, out, stream=N
     dt = DTYPE_F32 if out.dtype == torch.float32 else DTYPE_BF16
     _check(lib().swa_synth_tokens(seed, stream_id, layer, _ptr(req), _ptr(pos), req.numel(), heads,
                                   dim, dt, _ptr(out), _stream(stream)), None)
+
+
+# ------------------------------------------------- unified pool (two ends) ---
+UCTR_LOW, UCTR_HIGH, UCTR_REL_FULL, UCTR_REL_SWA, UCTR_VHEAD, UCTR_VCOUNT, UCTR_ERROR = range(7)
+
+
+class swa_unified_view(C.Structure):
+    _fields_ = [("v2p_full", C.c_void_p), ("v2p_swa", C.c_void_p),
+                ("released_full", C.c_void_p), ("released_swa", C.c_void_p),
+                ("virt_free", C.c_void_p), ("counters", C.c_void_p), ("num_pages", C.c_int64)]
+
+
+def _ucheck(status, handle):
+    if status != SWA_OK:
+        msg = lib().swa_unified_last_error(handle)
+        msg = msg.decode() if msg else ""
+        cls = SwaNoMem if status == SWA_ERR_NOMEM else SwaError
+        raise cls(status, msg)
+
+
+class UnifiedPool:
+    """Owns a swa_unified allocator and its device state blob."""
+
+    def __init__(self, num_pages, page_size, max_batch=64, device="cuda", stream=None):
+        n = lib().swa_unified_state_bytes(num_pages, max_batch)
+        if n == 0:
+            raise SwaError(SWA_ERR_INVALID, "bad unified pool size")
+        self.state = torch.empty(n, dtype=torch.uint8, device=device)
+        self.num_pages, self.page_size = int(num_pages), int(page_size)
+        h = C.c_void_p()
+        _ucheck(lib().swa_unified_create(num_pages, page_size, max_batch, _ptr(self.state),
+                                         _stream(stream), C.byref(h)), None)
+        self.handle = h
+
+    def __del__(self):
+        if getattr(self, "handle", None):
+            lib().swa_unified_destroy(self.handle)
+            self.handle = None
+
+    def _view(self):
+        v = swa_unified_view()
+        _ucheck(lib().swa_unified_state_pointers(self.handle, C.byref(v)), self.handle)
+        return v
+
+    def _tensor(self, ptr, n, dtype):
+        base = self.state.data_ptr()
+        off = ptr - base
+        item = torch.tensor([], dtype=dtype).element_size()
+        return self.state[off:off + n * item].view(dtype)
+
+    def v2p(self, full: bool):
+        v = self._view()
+        return self._tensor(v.v2p_full if full else v.v2p_swa, self.num_pages + 1, torch.int64)
+
+    def released(self, full: bool):
+        """Released page ids of one side, ascending (from its bitmap)."""
+        v = self._view()
+        words = (self.num_pages + 1 + 31) // 32
+        bm = self._tensor(v.released_full if full else v.released_swa, words, torch.int32)
+        bits = bm.cpu().numpy().view(np.uint32)
+        return [w * 32 + b for w in range(words) for b in range(32) if (int(bits[w]) >> b) & 1]
+
+    def counters(self):
+        v = self._view()
+        return self._tensor(v.counters, 8, torch.int64).cpu().tolist()
+
+    def virt_free(self):
+        """Free virtual page ids, front first."""
+        c = self.counters()
+        v = self._view()
+        ring = self._tensor(v.virt_free, self.num_pages, torch.int64).cpu().tolist()
+        head, count = c[UCTR_VHEAD], c[UCTR_VCOUNT]
+        return [ring[(head + i) % self.num_pages] for i in range(count)]
+
+
+def swa_unified_available_size(u):
+    return lib().swa_unified_available_size(u.handle)
+
+
+def swa_unified_sync(u, stream=None):
+    _ucheck(lib().swa_unified_sync(u.handle, _stream(stream)), u.handle)
+
+
+def swa_unified_device_check(u, stream=None):
+    err = C.c_int32()
+    st = lib().swa_unified_device_check(u.handle, _stream(stream), C.byref(err))
+    if st not in (SWA_OK, SWA_ERR_DEVICE_CHECK):
+        _ucheck(st, u.handle)
+    return err.value
+
+
+def swa_unified_alloc_extend(u, prefix_lens, seq_lens, last_loc, prefix_lens_host, seq_lens_host,
+                             out_virt, req_to_token=None, req_idx=None, stream=None):
+    bs = len(seq_lens_host)
+    ph, pp = _host(prefix_lens_host)
+    sh, sp = _host(seq_lens_host)
+    rt_stride = req_to_token.shape[1] if req_to_token is not None else 0
+    _ucheck(lib().swa_unified_alloc_extend(u.handle, bs, _ptr(prefix_lens), _ptr(seq_lens),
+                                           _ptr(last_loc), pp, sp, _ptr(out_virt),
+                                           _ptr(req_to_token), rt_stride, _ptr(req_idx),
+                                           _stream(stream)), u.handle)
+
+
+def swa_unified_free_swa(u, virt, stream=None):
+    _ucheck(lib().swa_unified_free_swa(u.handle, _ptr(virt), virt.numel(), _stream(stream)),
+            u.handle)
+
+
+def swa_unified_free(u, virt, stream=None):
+    _ucheck(lib().swa_unified_free(u.handle, _ptr(virt), virt.numel(), _stream(stream)), u.handle)
+
+
+def swa_unified_evict_swa(u, window_excl, req_to_token, req_idx, pre_lens, evicted, pre_lens_host,
+                          evicted_host, protected_lens=None, protected_host=None, interval=0,
+                          radix=False, stream=None):
+    """``evicted_host`` (numpy int64) is updated in place."""
+    bs = len(pre_lens_host)
+    ph, pp = _host(pre_lens_host)
+    assert isinstance(evicted_host, np.ndarray) and evicted_host.dtype == np.int64
+    assert evicted_host.flags["C_CONTIGUOUS"]
+    prh, prp = _host(protected_host)
+    _ucheck(lib().swa_unified_evict_swa(u.handle, bs, window_excl, _ptr(req_to_token),
+                                        req_to_token.shape[1], _ptr(req_idx), _ptr(pre_lens),
+                                        _ptr(evicted), _ptr(protected_lens), pp,
+                                        evicted_host.ctypes.data_as(C.c_void_p), prp, interval,
+                                        1 if radix else 0, _stream(stream)), u.handle)

@@ -309,9 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // of its earlier items) or item count n_done, so the rings run on across
   // items; each item ends with all roles joined (its Q tiles and TMEM free).
   int tg0 = 0, n_done = 0;
-  // Producer only: phases armed so far on each K / V "full" barrier, so that
-  // an abort can wait for the loads still in flight.
-  int armK[2] = {0, 0}, armV[2] = {0, 0};
+  // Producer only: running tile counts whose K / V loads were issued (tile T
+  // arms phase T >> 1 of "full" barrier T & 1), so that an abort can wait for
+  // the loads still in flight.
+  int k_issued = 0, v_issued = 0;
   for (int item = blockIdx.x; item < P.items_upper; item += gridDim.x) {
   __syncthreads();   // every thread has read the previous item's fields
   // ---- work item: two Q tiles of one request, latest first ----
@@ -406,7 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           const uint32_t full = bar((kv ? B_FULLV : B_FULLK) + s);
           mbar_expect_tx(full, (uint32_t)kTileBytes);   // every page slot is loaded
-          ++(kv ? armV : armK)[s];
+          if (kv) v_issued = T + 1;
+          else k_issued = T + 1;
           const uint32_t dst = sb + (kv ? kOffV : kOffK) + s * kTileBytes;
           for (int i = 0; i < pages_per_tile; ++i) {
             const int pi = t * pages_per_tile + i;
@@ -671,8 +673,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) set_error(P.err, SWA_DEVERR_TIMEOUT);
     if (warp == 9 && lane == 0) {
       for (int i = 0; i < 2; ++i) {
-        if (armK[i]) mbar_drain(bar(B_FULLK + i), (armK[i] - 1) & 1);
-        if (armV[i]) mbar_drain(bar(B_FULLV + i), (armV[i] - 1) & 1);
+        const int nk = (k_issued + 1 - i) >> 1, nv = (v_issued + 1 - i) >> 1;  // phases armed
+        if (nk) mbar_drain(bar(B_FULLK + i), (nk - 1) & 1);
+        if (nv) mbar_drain(bar(B_FULLV + i), (nv - 1) & 1);
       }
     }
     if (warp == 8 && lane == 0) {

@@ -59,6 +59,8 @@ class Spec:
     chunk: int = 8192
     description: str = ""
     seq_list: tuple = None   # explicit lengths (overrides seq_kind)
+    pools: tuple = None      # (size_full, size_swa) in tokens instead of the sizing rule
+    perm_free: bool = False  # pages handed out in a seeded permuted order
 
     def seq_lens(self) -> np.ndarray:
         if self.seq_list is not None:
@@ -87,6 +89,11 @@ EXTEND_PREFIX = 24576
 EXTEND_CHUNK = 8192
 
 SPECS = {
+    "tiny": Spec("tiny", [(SLIDING, 15, 1), (FULL, 0, 1)], 4, 64, "f32", 1, 2, "fixed", 0, 0, 0.25,
+                 8, 0, chunk=32, seq_list=(37, 200), pools=(512, 128), perm_free=True,
+                 description="Tiny: 1 sliding (W=16) + 1 full layer, 4 query heads, 1 KV head, D=64, "
+                 "fp32 KV, page 1, full pool 512 / SWA pool 128 slots in seeded permuted order, "
+                 "2 decode requests at seqlens 37 and 200, eviction interval 8"),
     "mimo": Spec("mimo", mimo_layers(), 64, 128, "bf16", 64, 64, "uniform", 4096, 32768, 0.8,
                  128, 1, description="MiMo-V2-Flash-shaped decode: 48 layers (39 sliding W=128 "
                  "with 8 KV heads, 9 full with 4 KV heads), 64 query heads, D=128, bf16 KV, "
@@ -138,7 +145,11 @@ class DecodeState:
         self.B = spec.batch
         self.max_steps = max_steps
         self.ps = spec.ps
-        nf, ns, M = sizing(spec, self.seq0, max_steps + spec.interval)
+        if spec.pools is not None:
+            nf, ns = spec.pools
+            M = 0
+        else:
+            nf, ns, M = sizing(spec, self.seq0, max_steps + spec.interval)
         self.swa_ring = swa_ring
         self.ring_size = 0
         if swa_ring:
@@ -179,10 +190,15 @@ class DecodeState:
                 self.swa_env[: 2 * ls * spec.ps * rb_s].fill_(0x7F)
             for kind, w, hkv in spec.layers:
                 gl.append(dict(kind=kind, window=w, num_kv_heads=hkv))
+        init_f = init_s = None
+        if spec.perm_free:
+            init_f = torch.tensor(synth.permutation(spec.seed + 101, nf // spec.ps), device=device)
+            init_s = torch.tensor(synth.permutation(spec.seed + 202, ns // spec.ps), device=device)
+        self.init_free = (init_f, init_s)
         self.ctx = api.SwaCtx(gl, spec.ps, nf, ns, spec.Hq, spec.D, DTYPES[spec.dtype],
                               api.LAYOUT_PER_LAYER if spec.layout == "per_layer"
                               else api.LAYOUT_ENVELOPE, False, max(self.B, 1),
-                              self.full_env, self.swa_env, device=device,
+                              self.full_env, self.swa_env, init_f, init_s, device=device,
                               ring_size=self.ring_size, ring_slots=(self.B + 1) if swa_ring else 0)
         self.rt = torch.zeros((self.B + 1, self.max_ctx), dtype=torch.int32, device=device)
         self.rows = np.arange(1, self.B + 1, dtype=np.int64)
@@ -345,39 +361,66 @@ class DecodeState:
         self.lens = inp["seq_h"].copy()
 
     # -- extend (one chunked-prefill round) -------------------------------------
-    def extend_round(self, chunk: int, attn_events=None, evict_events=None):
-        """One chunk of every request: eviction before the chunk, alloc_extend,
-        KV store, the per-batch plan and extend attention on every layer.
-        Returns the q tensors, outputs and metadata (kept for parity checks)."""
+    def make_extend_inputs(self, chunk: int):
+        """Everything one chunk round of every request reads that is not the
+        method's own state: the chunk's q/k/v of every layer (drawn on the
+        device), lengths, query offsets, the plan buffer and the workspace."""
         spec = self.spec
         pre = self.lens.copy()
         seq = pre + chunk
-        if evict_events:
-            evict_events[0].record()
-        self._evict(np.arange(self.B), 0)
-        if evict_events:
-            evict_events[1].record()
-        self._extend(np.arange(self.B), seq)
         ext = seq - pre
         indptr = np.concatenate([[0], np.cumsum(ext)]).astype(np.int64)
         n = int(indptr[-1])
         d = lambda x: torch.tensor(x, device=self.dev)
         meta = dict(pre=pre, seq=seq, indptr=indptr, n=n, pre_d=d(pre), seq_d=d(seq),
                     indptr_d=d(indptr))
-        plan = torch.zeros(api.swa_plan_bytes(self.ctx, self.B, int(ext.max())), dtype=torch.uint8,
-                           device=self.dev)
-        api.swa_plan(self.ctx, self.rt, self.rows_d, meta["pre_d"], meta["seq_d"], plan,
-                     int(ext.max()))
-        meta["plan"] = plan
+        meta["plan"] = torch.zeros(api.swa_plan_bytes(self.ctx, self.B, int(ext.max())),
+                                   dtype=torch.uint8, device=self.dev)
         reqs = torch.tensor(np.repeat(self.rows, ext), device=self.dev)
         pos = torch.tensor(np.concatenate([np.arange(p, s) for p, s in zip(pre, seq)]),
                            device=self.dev)
         meta["q"] = [self._synth(synth.STREAM_Q, l, reqs, pos, spec.Hq)
                      for l in range(len(spec.layers))]
+        meta["k"] = [self._synth(synth.STREAM_K, l, reqs, pos, h)
+                     for l, (_, _, h) in enumerate(spec.layers)]
+        meta["v"] = [self._synth(synth.STREAM_V, l, reqs, pos, h)
+                     for l, (_, _, h) in enumerate(spec.layers)]
         meta["out"] = [torch.empty_like(x) for x in meta["q"]]
+        meta["out_full"] = torch.empty(n, dtype=torch.int64, device=self.dev)
+        meta["out_swa"] = torch.empty(n, dtype=torch.int64, device=self.dev)
         wsb = max(api.swa_attn_extend_ws_bytes(self.ctx, l, n, int(seq.max()))
                   for l in range(len(spec.layers)))
         meta["ws"] = torch.zeros(wsb, dtype=torch.uint8, device=self.dev)
+        return meta
+
+    def extend_round(self, chunk: int, attn_events=None, evict_events=None, meta=None):
+        """One chunk of every request: eviction before the chunk, alloc_extend,
+        KV store of every layer, the per-batch plan and extend attention on
+        every layer, all on inputs prepared beforehand (``meta`` from
+        make_extend_inputs, drawn here when not given).  Returns ``meta``
+        with the outputs (kept for parity checks)."""
+        spec = self.spec
+        if meta is None:
+            meta = self.make_extend_inputs(chunk)
+        idx = np.arange(self.B)
+        if evict_events:
+            evict_events[0].record()
+        self._evict(idx, 0)
+        if evict_events:
+            evict_events[1].record()
+        pre, seq = meta["pre"], meta["seq"]
+        if self.trace is not None:
+            self.trace.append(("extend", self.rows.tolist(), pre.tolist(), seq.tolist()))
+        api.swa_alloc_extend(self.ctx, meta["pre_d"], meta["seq_d"], None, pre, seq,
+                             meta["out_full"], meta["out_swa"], req_to_token=self.rt,
+                             req_idx=self.rows_d)
+        for l in range(len(spec.layers)):
+            api.swa_store_kv(self.ctx, l, meta["k"][l], meta["v"][l], meta["out_full"],
+                             meta["out_swa"])
+        self.lens[idx] = seq
+        ext_max = int((seq - pre).max())
+        api.swa_plan(self.ctx, self.rt, self.rows_d, meta["pre_d"], meta["seq_d"], meta["plan"],
+                     ext_max)
         self.extend_attention(meta, attn_events)
         return meta
 

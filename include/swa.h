@@ -334,11 +334,96 @@ swa_status swa_alloc_decode(swa_ctx *ctx, int32_t bs, const int64_t *seq_lens,
  * the envelope layout; with v2p the identity this is the envelope's
  * kernel_id).  v2p: n_pages int64 on the device; virt, out: n int64 on the
  * device.  ctx may be NULL (then out-of-range virtual pages are only set to
- * 0); with a ctx they also set SWA_DEVERR_RANGE.  The allocation policy of
- * the unified pool behind v2p is not on the pages and not built here. */
+ * 0); with a ctx they also set SWA_DEVERR_RANGE.  The swa_unified_* calls
+ * below allocate a unified pool and fill its v2p tables. */
 swa_status swa_translate_for_kernel(swa_ctx *ctx, const int64_t *v2p, int64_t n_pages,
                                     const int64_t *virt, int64_t n, int32_t page_size,
                                     int32_t multiplier, int64_t *out, swa_stream_t stream);
+
+/* ------------------------------------------------- unified pool (two ends) --
+ * FULL and SWA sub-pools sharing one virtual id space and one physical page
+ * range, allocated from its two ends ([Pools 15], allocator-family table,
+ * UnifiedSWATokenToKVPoolAllocator, and the note on UnifiedSWAAllocatorBase:
+ * the shared ids replace the full->SWA table, the policy manages both
+ * budgets; [PR 34602], multi_ended_allocator.py: virtual_to_physical).
+ * Policy (this library's reading; the pages do not print one):
+ *   - physical pages 1..num_pages (page 0 is the sink of both sides).  FULL
+ *     takes pages upward from the low end, SWA downward from the high end;
+ *     the pages between the two frontiers are free to either side;
+ *   - a side reuses its released pages nearest its own end first (FULL the
+ *     lowest, SWA the highest), then grows its frontier; after a release a
+ *     frontier retracts over released pages of its side that border it;
+ *   - virtual pages 1..num_pages (owned by the FULL side) come from a free
+ *     ring, front first; released ids are prepended in ascending order;
+ *   - every new virtual page gets one FULL and one SWA physical page, written
+ *     to v2p_full[v] / v2p_swa[v]; a released SWA page leaves a tombstone -1
+ *     (kernel ids clamp it to the sink).
+ * A request's tokens get virtual slots v * page_size + t % page_size by the
+ * same rule as swa_alloc_extend (the open page continues after last_loc; new
+ * pages in request order); kernel-facing ids come from
+ * swa_translate_for_kernel(NULL, v2p_full or v2p_swa, num_pages + 1, ...).
+ * An allocation that needs n new pages fits iff n virtual pages are free and
+ * max(0, n - released_full) + max(0, n - released_swa) <= the gap; otherwise
+ * SWA_ERR_NOMEM and nothing changes.  Host mirror: exact after allocations;
+ * a release leaves it stale (a retraction depends on which pages came back),
+ * and the next allocation (or swa_unified_sync) reloads it with one stream
+ * synchronisation; swa_unified_available_size returns -1 while it is stale.
+ * State: caller-allocated device blob of swa_unified_state_bytes (256-byte
+ * aligned); views of it through swa_unified_state_pointers. */
+typedef struct swa_unified swa_unified;
+typedef struct swa_unified_view {
+  int64_t *v2p_full;          /* num_pages + 1 entries, -1 = none / tombstone  */
+  int64_t *v2p_swa;
+  uint32_t *released_full;    /* bitmap over page ids 0..num_pages             */
+  uint32_t *released_swa;
+  int64_t *virt_free;         /* ring of num_pages virtual page ids            */
+  int64_t *counters;          /* SWA_UCTR_*                                    */
+  int64_t num_pages;
+} swa_unified_view;
+enum swa_unified_counter {
+  SWA_UCTR_LOW = 0,       /* highest page FULL has taken from the low end       */
+  SWA_UCTR_HIGH = 1,      /* lowest page SWA has taken from the high end        */
+  SWA_UCTR_REL_FULL = 2,  /* released FULL pages (set bits of released_full)    */
+  SWA_UCTR_REL_SWA = 3,
+  SWA_UCTR_VHEAD = 4,     /* front of the virtual-id ring                       */
+  SWA_UCTR_VCOUNT = 5,    /* free virtual pages                                 */
+  SWA_UCTR_ERROR = 6      /* device error word (int32, swa_device_error bits)   */
+};
+size_t swa_unified_state_bytes(int64_t num_pages, int32_t max_batch);
+/* SWA_ERR_CONFIG when num_pages exceeds 1.7M or virtual slots would not fit
+ * req_to_token's int32. */
+swa_status swa_unified_create(int64_t num_pages, int32_t page_size, int32_t max_batch,
+                              void *state_dev, swa_stream_t stream, swa_unified **out);
+void swa_unified_destroy(swa_unified *u);
+const char *swa_unified_last_error(const swa_unified *u);
+swa_status swa_unified_state_pointers(const swa_unified *u, swa_unified_view *out);
+int64_t swa_unified_available_size(const swa_unified *u);
+swa_status swa_unified_sync(swa_unified *u, swa_stream_t stream);
+swa_status swa_unified_device_check(swa_unified *u, swa_stream_t stream, int32_t *err);
+/* Arguments as swa_alloc_extend; out_virt[sum(seq - pre)] receives virtual
+ * slots, and req_to_token (when given) holds virtual slots. */
+swa_status swa_unified_alloc_extend(swa_unified *u, int32_t bs, const int64_t *prefix_lens,
+                                    const int64_t *seq_lens, const int64_t *last_loc,
+                                    const int64_t *prefix_lens_host,
+                                    const int64_t *seq_lens_host, int64_t *out_virt,
+                                    int32_t *req_to_token, int64_t rt_stride,
+                                    const int64_t *req_idx, swa_stream_t stream);
+/* free_swa: releases the SWA page of each distinct virtual page of virt[n]
+ * that still has one (tombstone); free: free_swa, then the FULL page and the
+ * virtual page itself.  A virtual slot outside 1..num_pages pages sets
+ * SWA_DEVERR_RANGE and is skipped. */
+swa_status swa_unified_free_swa(swa_unified *u, const int64_t *virt, int64_t n,
+                                swa_stream_t stream);
+swa_status swa_unified_free(swa_unified *u, const int64_t *virt, int64_t n, swa_stream_t stream);
+/* swa_evict_swa's ranges ([SWA note], "runtime") with window_excl as Wx, over
+ * req_to_token holding virtual slots; each range's pages go through free_swa. */
+swa_status swa_unified_evict_swa(swa_unified *u, int32_t bs, int32_t window_excl,
+                                 const int32_t *req_to_token, int64_t rt_stride,
+                                 const int64_t *req_idx, const int64_t *pre_lens,
+                                 int64_t *evicted, const int64_t *protected_lens,
+                                 const int64_t *pre_lens_host, int64_t *evicted_host,
+                                 const int64_t *protected_host, int32_t interval, int32_t radix,
+                                 swa_stream_t stream);
 
 /* swa_translate: swa_loc[i] = full_to_swa[full_loc[i]], where full_loc -1
  * reads the trailing sentinel (-1) ([SWA note], "attention backend":

@@ -16,6 +16,9 @@ numpy / plain Python with float64 arithmetic for attention:
 * ``envelope``   - page-major envelope addressing (kernel-facing row ids).
 * ``hitrule``    - the W-contiguous-non-tombstone prefix-hit rule.
 * ``kvstore``    - per-layer / envelope KV pools that store and gather rows.
+* ``radix``      - the SWA component of the radix prefix cache.
+* ``unified``    - the unified FULL/SWA pool allocated from both ends of one
+                   page range, with its virtual-to-physical page tables.
 
 Source pages (cited by title and section throughout):
   [SWA note]      "SWA in SGLang" design note (zdszero.github.io/swa.html)

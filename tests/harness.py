@@ -315,10 +315,15 @@ OKIND = {FULL: OT.FULL, SLIDING: OT.SLIDING, CHUNKED: OT.CHUNKED}
 def replay(st: DecodeState):
     """The oracle allocator driven by the GPU state's recorded calls."""
     spec = st.spec
+    init_f = init_s = None
+    if spec.perm_free:      # the same seeded page order the GPU state was given
+        init_f = synth.permutation(spec.seed + 101, st.size_full // spec.ps)
+        init_s = synth.permutation(spec.seed + 202, st.size_swa // spec.ps)
     if st.swa_ring:
-        oa = OA.RingTwoPoolAllocator(st.size_full, spec.ps, st.ring_size, st.B + 1, spec.lookback())
+        oa = OA.RingTwoPoolAllocator(st.size_full, spec.ps, st.ring_size, st.B + 1, spec.lookback(),
+                                     False, init_f)
     else:
-        oa = OA.TwoPoolAllocator(st.size_full, st.size_swa, spec.ps)
+        oa = OA.TwoPoolAllocator(st.size_full, st.size_swa, spec.ps, False, init_f, init_s)
     ort = np.zeros(tuple(st.rt.shape), np.int64)
     for op in st.trace:
         if op[0] == "evict":

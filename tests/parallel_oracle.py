@@ -52,8 +52,20 @@ def attend_jobs(jobs, procs=None):
     n = procs or min(len(jobs), os.cpu_count() or 1, 32)
     if n <= 1:
         return [_run(j) for j in jobs]
-    with mp.get_context("spawn").Pool(n) as pool:
-        return pool.map(_run, jobs, chunksize=1)
+    # One BLAS thread per worker (the variables are read when a worker
+    # imports numpy, so they are set before the workers start).
+    keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {k: os.environ.get(k) for k in keys}
+    os.environ.update({k: "1" for k in keys})
+    try:
+        with mp.get_context("spawn").Pool(n) as pool:
+            return pool.map(_run, jobs, chunksize=1)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
 
 
 def decode_jobs(spec, layer, rows, seq_h, q_cpu, sinks_h, scale):
