@@ -1,6 +1,6 @@
 // Chunked-prefill (extend) attention on the 5th-generation tensor cores
-// (tcgen05 + TMEM + TMA), bf16 KV in the per-layer layout, D = 128, GQA group
-// G in {8, 16}, page size 16..128 (a power of two).
+// (tcgen05 + TMEM + TMA), bf16 KV in the per-layer layout, D = 64 or 128,
+// GQA group G in {8, 16}, page size 16..64 (a power of two).
 //
 // Method: "SWA in SGLang" design note - the chunk's queries at positions
 // pre..seq-1 attend causally; sliding layers see the last Wx+1 keys, full
@@ -15,10 +15,10 @@
 //   * all threads gather the Q rows once (cp.async) while the page rows are
 //     looked up; then warp 9, from one lane,
 //     streams K and V through a two-stage ring with TMA: one 3-D box
-//     {64 dims, 1 head, ps rows} per page and half of D, 128-byte swizzle,
+//     {64 dims, 1 head, ps rows} per page and 64-dim block of D, 128-byte swizzle,
 //     completion counted on "full" mbarriers, slots returned on "empty" ones;
 //   * warp 8 (one lane) issues tcgen05.mma: S_i = Q_i K^T into TMEM columns
-//     [128 i, 128 i + 128) and O_i += P_i V into columns [256 + 128 i, ...),
+//     [128 i, 128 i + 128) and O_i += P_i V into columns [256 + D i, ...),
 //     with P_i read from TMEM where it overwrote S_i, and tcgen05.commit for
 //     every hand-off;
 //   * warps 0-3 and 4-7 are the softmax groups of Q tile 0 and 1: each thread
@@ -47,12 +47,21 @@
 namespace swa {
 namespace {
 
-constexpr int kD = 128;
 constexpr int kRows = 128;                   // rows of one Q tile (M)
 constexpr int kKeys = 128;                   // keys per K/V tile
 constexpr int kThreads = 320;                // 8 softmax warps + MMA warp + load warp
-constexpr int kTileBytes = kRows * kD * 2;   // 128 x 128 bf16 = 32 KB
-constexpr int kHalf = kTileBytes / 2;        // one 64-column block
+constexpr int kBlock = kRows * 64 * 2;       // one 64-column block of a 128-row tile (16 KB)
+// A 128-row (or 128-key) tile of D bf16 columns: D / 64 blocks of
+// [128 rows][128 B] with the 128-byte swizzle.
+template <int D>
+struct Geo {
+  static constexpr int kTileBytes = kRows * D * 2;
+  static constexpr int kOffQ = 0;                  // Q0, Q1
+  static constexpr int kOffK = 2 * kTileBytes;     // K stage 0, 1
+  static constexpr int kOffV = 4 * kTileBytes;     // V stage 0, 1
+  static constexpr int kOffRows = 6 * kTileBytes;  // int32 page rows [max_pages]
+  static constexpr int kCPR = D / 8;               // 16-byte chunks of a row
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr long kSpinLimit = 1L << 24;
 constexpr float kRescaleGap = 8.f;           // log2 units: rescale O when the max grows more
@@ -242,7 +251,7 @@ __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sy
 // (row r, 16-byte chunk c in 0..15) of a 128 x 128 bf16 tile stored as two
 // 64-column blocks of [128 rows][128 B] with the 128-byte swizzle.
 __device__ __forceinline__ uint32_t tile_off(int r, int c) {
-  return (uint32_t)((c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+  return (uint32_t)((c >> 3) * kBlock + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 __device__ __forceinline__ int64_t key_lo(int kind, int window, int64_t p) {
@@ -251,17 +260,17 @@ __device__ __forceinline__ int64_t key_lo(int kind, int window, int64_t p) {
   return (p / window) * window;
 }
 
-// Shared memory (offsets from a 1024-byte aligned base).
-constexpr int kOffQ = 0;                        // Q0, Q1
-constexpr int kOffK = 2 * kTileBytes;           // K stage 0, 1
-constexpr int kOffV = 4 * kTileBytes;           // V stage 0, 1
-constexpr int kOffRows = 6 * kTileBytes;        // int32 page rows [max_pages]
+// Shared memory (offsets from a 1024-byte aligned base): Geo<D>.
 enum { B_FULLK = 0, B_EMPTYK = 2, B_FULLV = 4, B_EMPTYV = 6, B_SDONE = 8, B_PREADY = 10,
        B_ODONE = 12, B_DRAIN = 13, B_COUNT = 14 };
 
+template <int kD>
 __global__ void __launch_bounds__(kThreads, 1)
     k_extend_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 TcParams P) {
+  using Gm = Geo<kD>;
+  constexpr int kTileBytes = Gm::kTileBytes, kOffQ = Gm::kOffQ, kOffK = Gm::kOffK;
+  constexpr int kOffV = Gm::kOffV, kOffRows = Gm::kOffRows, kCPR = Gm::kCPR;
   extern __shared__ char smem_raw[];
   char *smem = reinterpret_cast<char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(smem);
@@ -302,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   constexpr uint32_t kIdS = idesc_f16(128, 128, false);
-  constexpr uint32_t kIdO = idesc_f16(128, 128, true);
+  constexpr uint32_t kIdO = idesc_f16(128, kD, true);
 
   // Persistent: the CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...
   // Every barrier phase follows the CTA's running tile count tg0 (key tiles
@@ -353,8 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the chunk); their latency overlaps the page-row lookups below.
   {
     const int Hq = P.hkv * G;
-    for (int i = tid; i < 2 * kRows * 16; i += kThreads) {
-      const int qt = i / (kRows * 16), rr = (i / 16) % kRows, c = i % 16;
+    for (int i = tid; i < 2 * kRows * kCPR; i += kThreads) {
+      const int qt = i / (kRows * kCPR), rr = (i / kCPR) % kRows, c = i % kCPR;
       const int64_t tok = q0 + qt * T + rr / G;
       const bool ok = tok < s_qend && (qt * T + rr / G) < n_tok;
       const __nv_bfloat16 *src = P.q + ((ok ? tok : q0) * Hq + kvh * G + rr % G) * kD + c * 8;
@@ -413,8 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < pages_per_tile; ++i) {
             const int pi = t * pages_per_tile + i;
             const int32_t row = s_rows[pi] >= 0 ? s_rows[pi] : s_rows[slot_lo];
-            for (int h = 0; h < 2; ++h)
-              tma_load_3d(dst + h * kHalf + i * P.ps * 128, kv ? &tmV : &tmK, h * 64, kvh, row, full);
+            for (int h = 0; h < kD / 64; ++h)
+              tma_load_3d(dst + h * kBlock + i * P.ps * 128, kv ? &tmV : &tmK, h * 64, kvh, row, full);
           }
         }
       }
@@ -432,13 +441,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dq1 = smem_desc(sb + kOffQ + kTileBytes, 16, 1024);
     const uint64_t dk0 = smem_desc(sb + kOffK, 16, 1024);
     const uint64_t dk1 = smem_desc(sb + kOffK + kTileBytes, 16, 1024);
-    const uint64_t dv0 = smem_desc(sb + kOffV, kHalf, 1024);
-    const uint64_t dv1 = smem_desc(sb + kOffV + kTileBytes, kHalf, 1024);
+    const uint64_t dv0 = smem_desc(sb + kOffV, kBlock, 1024);
+    const uint64_t dv1 = smem_desc(sb + kOffV + kTileBytes, kBlock, 1024);
     auto issue_s = [&](int i, int T) {     // T: running tile count (stage)
       const uint64_t qd = i ? dq1 : dq0, kd = (T & 1) ? dk1 : dk0;
 #pragma unroll
       for (int ks = 0; ks < kD / 16; ++ks) {
-        const uint64_t off16 = ((ks >> 2) * kHalf + (ks & 3) * 32) >> 4;
+        const uint64_t off16 = ((ks >> 2) * kBlock + (ks & 3) * 32) >> 4;
         mma_ss(tmem + i * 128, qd + off16, kd + off16, kIdS, ks > 0);
       }
       tc_commit(bar(B_SDONE + i));
@@ -447,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t vd = (T & 1) ? dv1 : dv0;
 #pragma unroll
       for (int ks = 0; ks < kKeys / 16; ++ks)
-        mma_ts(tmem + 256 + i * 128, tmem + i * 128 + ks * 8, vd + (uint64_t)(ks * 16 * 128 >> 4),
+        mma_ts(tmem + 256 + i * kD, tmem + i * 128 + ks * 8, vd + (uint64_t)(ks * 16 * 128 >> 4),
                kIdO, (t > 0 || ks > 0) ? 1u : 0u);
     };
     if (lane == 0 && mbar_wait(bar(B_FULLK + (tg0 & 1)), (tg0 >> 1) & 1, &s_abort)) {
@@ -489,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t lo_row = key_lo(P.kind, P.window, p_row);
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + grp * 128 + lane_off;
-    const uint32_t tO = tmem + 256 + grp * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + grp * kD + lane_off;
     float m_run = -INFINITY, l_run = 0.f;
     bool alive = true;
     for (int t = 0; t < n_tiles; ++t) {
@@ -624,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The warp's 32 output rows go through shared memory (the Q tile area:
       // every product that read it has completed by ODONE), so that the global
       // stores are whole 256-byte rows written by 16 consecutive lanes.
-      char *stage = smem + kOffQ + grp * kTileBytes + (warp & 3) * 32 * 256;
+      char *stage = smem + kOffQ + grp * kTileBytes + (warp & 3) * 32 * (kD * 2);
 #pragma unroll 1
       for (int cb = 0; cb < kD / 64; ++cb) {
         uint32_t rr[64];
@@ -641,18 +650,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             w[k] = *reinterpret_cast<uint32_t *>(&h);
           }
           const int c = (cb * 64 + e) >> 3;   // 16-byte chunk of the row
-          *reinterpret_cast<uint4 *>(stage + lane * 256 + ((c ^ (lane & 15)) << 4)) =
+          *reinterpret_cast<uint4 *>(stage + lane * (kD * 2) + ((c ^ (lane & (kCPR - 1))) << 4)) =
               make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       __syncwarp();
 #pragma unroll 4
-      for (int idx = lane; idx < 32 * 16; idx += 32) {
-        const int i = idx >> 4, c = idx & 15;
+      for (int idx = lane; idx < 32 * kCPR; idx += 32) {
+        const int i = idx / kCPR, c = idx % kCPR;
         const int rw = (warp & 3) * 32 + i;     // row of Q tile grp
         const int trw = grp * T + rw / G;
         if (trw < n_tok) {
-          const uint4 v = *reinterpret_cast<const uint4 *>(stage + i * 256 + ((c ^ (i & 15)) << 4));
+          const uint4 v =
+              *reinterpret_cast<const uint4 *>(stage + i * (kD * 2) + ((c ^ (i & (kCPR - 1))) << 4));
           *reinterpret_cast<uint4 *>(P.out + ((q0 + trw) * Hq + kvh * G + rw % G) * kD + c * 8) = v;
         }
       }
@@ -693,9 +703,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+template <int D>
+cudaError_t launch_d(dim3 grid, size_t tail, const LayerInfo &L, const TcParams &P, cudaStream_t s) {
+  const size_t smem = 1024 + Geo<D>::kOffRows + tail;
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  cudaError_t e =
+      cudaFuncSetAttribute(k_extend_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k_extend_tc<D><<<grid, kThreads, smem, s>>>(L.tmk, L.tmv, P);
+  return cudaGetLastError();
+}
+
 bool tc_extend_supported(const Ctx &c, int layer) {
-  if (!c.layers[layer].tma || c.cfg.kv_dtype != SWA_DTYPE_BF16 || c.cfg.head_dim != kD ||
-      c.cfg.page_size > 64)
+  if (!c.layers[layer].tma || c.cfg.kv_dtype != SWA_DTYPE_BF16 ||
+      (c.cfg.head_dim != 64 && c.cfg.head_dim != 128) || c.cfg.page_size > 64)
     return false;
   const int G = c.cfg.num_q_heads / c.layers[layer].hkv;
   return G == 8 || G == 16;
@@ -730,17 +751,13 @@ cudaError_t launch_attn_extend_tc(Ctx &c, const AttnArgs &a, cudaStream_t s) {
   P.out = static_cast<__nv_bfloat16 *>(a.out);
   P.max_pages = a.max_seq_len / P.ps + kKeys / P.ps + 2;
   P.err = c.err_word;
-  const size_t smem = 1024 + kOffRows + ((size_t)P.max_pages * 4 + 7) / 8 * 8 + B_COUNT * 8;
-  if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e =
-      cudaFuncSetAttribute(k_extend_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   // Persistent: one CTA per SM (the KV heads share the SMs), each looping
   // over its items.
   const int per_head = std::max(1, (c.num_sms > 0 ? c.num_sms : 148) / L.hkv);
   dim3 grid(std::min(P.items_upper, per_head), L.hkv);
-  k_extend_tc<<<grid, kThreads, smem, s>>>(L.tmk, L.tmv, P);
-  return cudaGetLastError();
+  const size_t tail = ((size_t)P.max_pages * 4 + 7) / 8 * 8 + B_COUNT * 8;
+  if (c.cfg.head_dim == 64) return launch_d<64>(grid, tail, L, P, s);
+  return launch_d<128>(grid, tail, L, P, s);
 }
 
 }  // namespace swa

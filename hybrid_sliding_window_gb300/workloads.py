@@ -220,16 +220,22 @@ class DecodeState:
         api.swa_synth_tokens(self.spec.seed, stream_id, layer, req_d, pos_d, heads, self.spec.D, out)
         return out
 
-    def _evict(self, idx, interval):
-        """Eviction pass over batch entries idx (numpy)."""
+    def _evict(self, idx, interval, events=None):
+        """Eviction pass over batch entries idx (numpy); ``events`` (start,
+        end) are recorded around the library call alone."""
         idx_d = torch.tensor(idx, device=self.dev)
         ev_h = self.evicted[idx].copy()
         ev_d = self.evicted_d[idx_d].contiguous()
         pre = self.lens[idx].copy()
+        rows_d = self.rows_d[idx_d].contiguous()
+        pre_d = torch.tensor(pre, device=self.dev)
         if self.trace is not None:
             self.trace.append(("evict", self.rows[idx].tolist(), pre.tolist(), ev_h.tolist(), interval))
-        api.swa_evict_swa(self.ctx, self.rt, self.rows_d[idx_d].contiguous(),
-                          torch.tensor(pre, device=self.dev), ev_d, pre, ev_h, interval=interval)
+        if events:
+            events[0].record()
+        api.swa_evict_swa(self.ctx, self.rt, rows_d, pre_d, ev_d, pre, ev_h, interval=interval)
+        if events:
+            events[1].record()
         self.evicted[idx] = ev_h
         self.evicted_d[idx_d] = ev_d
 
@@ -403,11 +409,7 @@ class DecodeState:
         if meta is None:
             meta = self.make_extend_inputs(chunk)
         idx = np.arange(self.B)
-        if evict_events:
-            evict_events[0].record()
-        self._evict(idx, 0)
-        if evict_events:
-            evict_events[1].record()
+        self._evict(idx, 0, evict_events)
         pre, seq = meta["pre"], meta["seq"]
         if self.trace is not None:
             self.trace.append(("extend", self.rows.tolist(), pre.tolist(), seq.tolist()))

@@ -16,10 +16,11 @@ from oracle import attention as OT  # noqa: E402
 from tests.harness import Pair, assert_close  # noqa: E402
 
 LAYERS = [(OT.SLIDING, 127, 8), (OT.FULL, 0, 4)]
+GPTOSS_LAYERS = [(OT.SLIDING, 127, 8), (OT.FULL, 0, 8)]      # G = 8, D = 64
 
 
-def _run(ps, path, prompt, chunk, layers=LAYERS, chunk0=256):
-    P = Pair(layers, Hq=64, D=128, dtype="bf16", ps=ps, size_full=ps * (4096 // ps + 40),
+def _run(ps, path, prompt, chunk, layers=LAYERS, chunk0=256, D=128):
+    P = Pair(layers, Hq=64, D=D, dtype="bf16", ps=ps, size_full=ps * (4096 // ps + 40),
              size_swa=ps * (1536 // ps + 40), seed=11, perm_free=True, max_ctx=4096, max_reqs=4)
     api.swa_set_attn_path(P.ctx, path)
     rows = [1, 2, 3]
@@ -59,3 +60,18 @@ def test_extend_long_prefix_many_key_tiles():
     assert api.swa_last_attn_path(P.ctx) == 2
     for l, (g, o) in res.items():
         assert_close(g, o, 2e-2, f"layer {l}")
+
+
+@pytest.mark.parametrize("ps", [16, 64])
+@pytest.mark.parametrize("path,expect", [pytest.param(-1, 2, id="tcgen05"),
+                                         pytest.param(0, 0, id="generic")])
+def test_extend_gptoss_shaped_head_dim_64(ps, path, expect):
+    """GPT-OSS-shaped layers (D = 64, 8 KV heads, G = 8): the tensor-core
+    kernel's 64-column tiles, many key tiles, mid-page prefixes, an empty
+    prefix and evicted SWA KV below the window."""
+    P, res = _run(ps, path, prompt=[1500, 333, 0], chunk=[150, 77, 40], layers=GPTOSS_LAYERS,
+                  D=64)
+    assert api.swa_last_attn_path(P.ctx) == expect
+    for l, (g, o) in res.items():
+        assert_close(g, o, 2e-2, f"D=64 ps={ps} layer {l}")
+    assert api.swa_device_check(P.ctx) == 0

@@ -131,15 +131,22 @@ def _model_rows(P, l, rows, pre, seq, heads):
 # ---------------------------------------------------------------------------
 # extend
 # ---------------------------------------------------------------------------
-EXTEND_LAYERS = [(OT.SLIDING, 127, 8), (OT.FULL, 0, 4)]
+EXTEND_SHAPES = {
+    # MiMo-shaped: D = 128, full layer G = 16, page 64
+    "mimo": dict(layers=[(OT.SLIDING, 127, 8), (OT.FULL, 0, 4)], D=128, ps=64),
+    # GPT-OSS-shaped: D = 64, G = 8, page 16
+    "gptoss": dict(layers=[(OT.SLIDING, 127, 8), (OT.FULL, 0, 8)], D=64, ps=16),
+}
 
 
+@pytest.mark.parametrize("shape", list(EXTEND_SHAPES))
 @pytest.mark.parametrize("variant", ["q16", "k-sawtooth"])
 @pytest.mark.parametrize("path,expect", [pytest.param(-1, 2, id="tcgen05"),
                                          pytest.param(0, 0, id="generic")])
-def test_extend_wide_scores(variant, path, expect):
-    ps = 64
-    P = Pair(EXTEND_LAYERS, Hq=64, D=128, dtype="bf16", ps=ps, size_full=ps * (4096 // ps + 40),
+def test_extend_wide_scores(shape, variant, path, expect):
+    c = EXTEND_SHAPES[shape]
+    ps = c["ps"]
+    P = Pair(c["layers"], Hq=64, D=c["D"], dtype="bf16", ps=ps, size_full=ps * (4096 // ps + 40),
              size_swa=ps * (1536 // ps + 40), seed=21, perm_free=True, max_ctx=4096, max_reqs=4)
     api.swa_set_attn_path(P.ctx, path)
     if variant == "q16":
@@ -156,7 +163,7 @@ def test_extend_wide_scores(variant, path, expect):
     assert api.swa_last_attn_path(P.ctx) == expect
     for l, (g, o) in res.items():
         assert np.isfinite(g).all(), f"layer {l}: non-finite output"
-        assert_close(g, o, TOL["bf16"], f"{variant} layer {l}")
+        assert_close(g, o, TOL["bf16"], f"{shape} {variant} layer {l}")
     assert api.swa_device_check(P.ctx) == 0
     if path == -1:
         # The inputs drive the rescale on both blocks of a tile, and a loop
