@@ -9,9 +9,12 @@
 // current token) or floor(p / C) * C..p (chunked local); a per-head sink
 // logit joins the softmax denominator only.
 //
-// Work item = (query, KV head, split of SPLIT keys).  A CTA of 4 warps keeps
-// one online-softmax state per warp for the G query heads of its KV head
-// (scores in log2 units), merges the warps in shared memory, and either
+// Work item = (query, KV head, split of SPLIT keys).  A CTA first looks up
+// the KV rows of all keys of its split (one independent load per key, all
+// threads), then 4 warps each walk every 4th key keeping one online-softmax
+// state for the G query heads of its KV head (scores in log2 units), with the
+// K/V rows of their next 4 keys loaded before any is used; it merges the
+// warps in shared memory, and either
 // writes the output (one split) or a partial (m, l, acc); the last CTA of a
 // (query, KV head) to finish - found with an atomic ticket - merges the
 // partials, folds in the sink and resets the ticket, so one launch does both.
@@ -132,6 +135,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_attn_simt(SimtParams P) {
   __shared__ float qs[kGMax][D];
   __shared__ float sm_m[kWarps][kGMax], sm_l[kWarps][kGMax];
   __shared__ float sm_acc[kWarps][kGMax][D];
+  __shared__ int64_t s_row[kSplit];
   __shared__ int s_last;
 
   const QT *qp = static_cast<const QT *>(P.q);
@@ -139,6 +143,16 @@ __global__ void __launch_bounds__(kWarps * 32) k_attn_simt(SimtParams P) {
   for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
     int g = e / D, d = e % D;
     qs[g][d] = qload<QT>(qp, ((int64_t)qi * Hq + kvh * G + g) * D + d) * P.scale_log2;
+  }
+  // KV rows of the split's keys, looked up once (independent loads).
+  const int nk = (int)(k1 - k0);
+  for (int i = threadIdx.x; i < nk; i += blockDim.x) {
+    int64_t slot = slot_of(P, b, k0 + i);
+    if (slot < 0 || slot >= P.pool_rows) {
+      set_error(P.err, SWA_DEVERR_RANGE);
+      slot = 0;
+    }
+    s_row[i] = kv_row(P.addr, slot);
   }
   __syncthreads();
 
@@ -151,36 +165,42 @@ __global__ void __launch_bounds__(kWarps * 32) k_attn_simt(SimtParams P) {
     for (int e = 0; e < DL; ++e) acc[g][e] = 0.f;
   }
   const float ksc = P.k_scale, vsc = P.v_scale;
-  for (int64_t j = k0 + warp; j < k1; j += kWarps) {
-    int64_t slot = slot_of(P, b, j);
-    if (slot < 0 || slot >= P.pool_rows) {
-      set_error(P.err, SWA_DEVERR_RANGE);
-      slot = 0;
+  constexpr int kAhead = 4;   // keys of one warp whose K/V rows are in flight together
+  for (int i0 = warp; i0 < nk; i0 += kWarps * kAhead) {
+    float kf[kAhead][DL], vf[kAhead][DL];
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u) {
+      const int i = i0 + u * kWarps;
+      if (i < nk) {
+        const int64_t row = s_row[i];
+        const KT *kr = reinterpret_cast<const KT *>(P.addr.k + row * P.addr.row_bytes) + kvh * D + lane * DL;
+        const KT *vr = reinterpret_cast<const KT *>(P.addr.v + row * P.addr.row_bytes) + kvh * D + lane * DL;
+#pragma unroll
+        for (int e = 0; e < DL; ++e) {
+          kf[u][e] = Elem<KT>::get(kr, e) * ksc;
+          vf[u][e] = Elem<KT>::get(vr, e) * vsc;
+        }
+      }
     }
-    const int64_t row = kv_row(P.addr, slot);
-    const KT *kr = reinterpret_cast<const KT *>(P.addr.k + row * P.addr.row_bytes) + kvh * D + lane * DL;
-    const KT *vr = reinterpret_cast<const KT *>(P.addr.v + row * P.addr.row_bytes) + kvh * D + lane * DL;
-    float kf[DL], vf[DL];
 #pragma unroll
-    for (int e = 0; e < DL; ++e) {
-      kf[e] = Elem<KT>::get(kr, e) * ksc;
-      vf[e] = Elem<KT>::get(vr, e) * vsc;
-    }
+    for (int u = 0; u < kAhead; ++u) {
+      if (i0 + u * kWarps >= nk) break;
 #pragma unroll
-    for (int g = 0; g < kGMax; ++g) {
-      if (g < G) {
-        float s = 0.f;
+      for (int g = 0; g < kGMax; ++g) {
+        if (g < G) {
+          float s = 0.f;
 #pragma unroll
-        for (int e = 0; e < DL; ++e) s += qs[g][lane * DL + e] * kf[e];
+          for (int e = 0; e < DL; ++e) s += qs[g][lane * DL + e] * kf[u][e];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        float mn = fmaxf(m[g], s);
-        float corr = exp2f(m[g] - mn);
-        float pe = exp2f(s - mn);
-        l[g] = l[g] * corr + pe;
+          for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+          float mn = fmaxf(m[g], s);
+          float corr = exp2f(m[g] - mn);
+          float pe = exp2f(s - mn);
+          l[g] = l[g] * corr + pe;
 #pragma unroll
-        for (int e = 0; e < DL; ++e) acc[g][e] = acc[g][e] * corr + pe * vf[e];
-        m[g] = mn;
+          for (int e = 0; e < DL; ++e) acc[g][e] = acc[g][e] * corr + pe * vf[u][e];
+          m[g] = mn;
+        }
       }
     }
   }
