@@ -29,7 +29,8 @@ namespace swa {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kSplit = 512;
+constexpr int kSplit = 512;      // longest split (the row table in shared memory)
+constexpr int kMinSplit = 32;
 constexpr int kGMax = 16;
 constexpr float kNegBig = -1e30f;
 
@@ -53,6 +54,7 @@ struct SimtParams {
   float *partials;
   int32_t *tickets;
   int max_splits;
+  int split_keys;             // keys per split, a power of two in [kMinSplit, kSplit]
   int32_t *err;
 };
 
@@ -127,10 +129,10 @@ __global__ void __launch_bounds__(kWarps * 32) k_attn_simt(SimtParams P) {
   locate_query(P, qi, b, p);
   const int64_t lo = key_lo(P.kind, P.window, p);
   const int64_t n_keys = p - lo + 1;
-  const int n_splits = (int)((n_keys + kSplit - 1) / kSplit);
+  const int n_splits = (int)((n_keys + P.split_keys - 1) / P.split_keys);
   if (split >= n_splits) return;
-  const int64_t k0 = lo + (int64_t)split * kSplit;
-  const int64_t k1 = min(p + 1, k0 + kSplit);
+  const int64_t k0 = lo + (int64_t)split * P.split_keys;
+  const int64_t k1 = min(p + 1, k0 + P.split_keys);
 
   __shared__ float qs[kGMax][D];
   __shared__ float sm_m[kWarps][kGMax], sm_l[kWarps][kGMax];
@@ -180,11 +182,16 @@ __global__ void __launch_bounds__(kWarps * 32) k_attn_simt(SimtParams P) {
           kf[u][e] = Elem<KT>::get(kr, e) * ksc;
           vf[u][e] = Elem<KT>::get(vr, e) * vsc;
         }
+      } else {
+#pragma unroll
+        for (int e = 0; e < DL; ++e) kf[u][e] = vf[u][e] = 0.f;
       }
     }
+    // Scores of the keys first (independent reductions, in flight
+    // together), then the online-softmax updates in key order.
+    float sc[kAhead][kGMax];
 #pragma unroll
     for (int u = 0; u < kAhead; ++u) {
-      if (i0 + u * kWarps >= nk) break;
 #pragma unroll
       for (int g = 0; g < kGMax; ++g) {
         if (g < G) {
@@ -193,6 +200,17 @@ __global__ void __launch_bounds__(kWarps * 32) k_attn_simt(SimtParams P) {
           for (int e = 0; e < DL; ++e) s += qs[g][lane * DL + e] * kf[u][e];
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+          sc[u][g] = s;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u) {
+      if (i0 + u * kWarps >= nk) break;
+#pragma unroll
+      for (int g = 0; g < kGMax; ++g) {
+        if (g < G) {
+          const float s = sc[u][g];
           float mn = fmaxf(m[g], s);
           float corr = exp2f(m[g] - mn);
           float pe = exp2f(s - mn);
@@ -292,13 +310,23 @@ struct WsLayout {
   size_t part_off;
   size_t total;
   int max_splits;
+  int split_keys;
 };
 
 WsLayout ws_layout(const Ctx &c, int layer, int64_t nq, int max_seq_len) {
   WsLayout w;
   const LayerInfo &L = c.layers[layer];
   const int G = c.cfg.num_q_heads / L.hkv;
-  w.max_splits = (max_keys(c, layer, max_seq_len) + kSplit - 1) / kSplit;
+  // Split size: the longest (kSplit) unless the launch would then fill less
+  // than one wave of 2 CTAs per SM; small batches cut their keys finer so
+  // more CTAs walk them in parallel (partials merged in the same launch).
+  const int mk = max_keys(c, layer, max_seq_len);
+  const int64_t slots = 2LL * (c.num_sms > 0 ? c.num_sms : 148);
+  w.split_keys = kSplit;
+  while (w.split_keys > kMinSplit &&
+         nq * L.hkv * ((mk + w.split_keys - 1) / w.split_keys) < slots)
+    w.split_keys /= 2;
+  w.max_splits = (mk + w.split_keys - 1) / w.split_keys;
   w.partial_bytes = (size_t)nq * L.hkv * w.max_splits * G * (c.cfg.head_dim + 2) * sizeof(float);
   w.part_off = ws_partials_off(c, nq);   // [reserved][tickets][partials]
   w.total = w.part_off + (w.partial_bytes + 255) / 256 * 256;
@@ -353,6 +381,7 @@ cudaError_t launch_attn_simt(Ctx &c, const AttnArgs &a, cudaStream_t s) {
   P.partials = reinterpret_cast<float *>(static_cast<char *>(a.ws) + w.part_off);
   P.tickets = reinterpret_cast<int32_t *>(static_cast<char *>(a.ws) + 256);
   P.max_splits = w.max_splits;
+  P.split_keys = w.split_keys;
   P.err = c.err_word;
   dim3 grid(w.max_splits, L.hkv, a.nq);
   if (c.cfg.kv_dtype == SWA_DTYPE_F32) return dispatch_dl<float, float>(P.D, grid, P, s);
