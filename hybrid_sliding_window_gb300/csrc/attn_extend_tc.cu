@@ -552,9 +552,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           m2[(e >> 1) & 3] = max3(m2[(e >> 1) & 3], __uint_as_float(rr[e]), __uint_as_float(rr[e + 1]));
         float cm = max3(m2[0], m2[1], fmaxf(m2[2], m2[3]));
         cm = cm == -INFINITY ? -INFINITY : cm * sc;
+        // A row whose maximum is still -inf has accumulated exactly nothing
+        // (every P so far was 0), so its first finite maximum needs no
+        // rescale (factor 1): only moves of a finite maximum pay for one.
         float corr = 1.f;
         if (cm > m_run + kRescaleGap || (m_run == -INFINITY && cm != -INFINITY)) {
-          corr = m_run == -INFINITY ? 0.f : exp2f(m_run - cm);
+          corr = m_run == -INFINITY ? 1.f : exp2f(m_run - cm);
           m_run = cm;
         }
         if (__any_sync(0xffffffffu, corr != 1.f)) {
