@@ -289,8 +289,12 @@ __global__ void __launch_bounds__(NW * 32, (Smem<D, FP8, KM, NW>::kMinBlocks))
   const int Hq = P.hkv * G;
 
   // Launched as a programmatic dependent of the previous kernel on the
-  // stream: wait for it (and its memory) before the first global access.
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  // stream.  The index tables read first (sequence length, plan, req_to_token)
+  // come from the allocation and plan kernels, which completed before the
+  // previous kernel passed its own wait, so they are read before this
+  // kernel's wait and their latency overlaps the previous kernel's tail;
+  // everything the previous kernel may write (q, the new token's K/V, the
+  // workspace) and the tile loads come after the wait.
   const ReqRef R = req_ref(P, b);
   // Windowed layers whose plan row fits one warp: the row's page entries are
   // read now, with the sequence length and the plan header, instead of after
@@ -309,18 +313,6 @@ __global__ void __launch_bounds__(NW * 32, (Smem<D, FP8, KM, NW>::kMinBlocks))
   const int64_t k0 = lo + (int64_t)split * P.split_keys;
   const int64_t k1 = min(p + 1, k0 + P.split_keys);
   const int n_tiles = (int)((k1 - k0 + kTile - 1) / kTile);
-
-  // ---- Q rows into registers: their latency hides behind the page-row
-  // lookups and the first tile loads ----
-  constexpr int kQPer = 16 * (D / 8) / (kWarps * 32);
-  uint4 qv[kQPer];
-#pragma unroll
-  for (int k = 0; k < kQPer; ++k) {
-    const int i = tid + k * kWarps * 32;
-    const int r = i / (D / 8), c = i % (D / 8);
-    qv[k] = make_uint4(0, 0, 0, 0);
-    if (r < G) qv[k] = *reinterpret_cast<const uint4 *>(P.q + ((int64_t)b * Hq + kvh * G + r) * D + c * 8);
-  }
 
   // ---- pages of this split, looked up once (one table read per page) ----
   // Positions of one page occupy consecutive slots of one pool page, so key j
@@ -365,6 +357,21 @@ __global__ void __launch_bounds__(NW * 32, (Smem<D, FP8, KM, NW>::kMinBlocks))
       page = 0;
     }
     s_rb[i] = page * page_stride * rb;
+  }
+
+  // The previous kernel's memory is needed from here on.
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+
+  // ---- Q rows into registers: their latency hides behind the first tile
+  // loads ----
+  constexpr int kQPer = 16 * (D / 8) / (kWarps * 32);
+  uint4 qv[kQPer];
+#pragma unroll
+  for (int k = 0; k < kQPer; ++k) {
+    const int i = tid + k * kWarps * 32;
+    const int r = i / (D / 8), c = i % (D / 8);
+    qv[k] = make_uint4(0, 0, 0, 0);
+    if (r < G) qv[k] = *reinterpret_cast<const uint4 *>(P.q + ((int64_t)b * Hq + kvh * G + r) * D + c * 8);
   }
 
   // ---- tile loader ----
