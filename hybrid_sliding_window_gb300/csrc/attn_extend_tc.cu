@@ -8,13 +8,21 @@
 //
 // GB300 design (persistent: one CTA per SM loops over work items; 10 warps,
 // warp-specialised; TMEM and barriers set up once per CTA, barrier phases
-// following the CTA's running tile count across items):
+// following running counts, so that no role waits for the others at an item
+// boundary):
 //   * an item is two 128-row Q tiles, each (128/G) consecutive query tokens
 //     x the G query heads of one KV head, so every K/V tile it loads feeds two
 //     QK^T and two PV products;
-//   * all threads gather the Q rows once (cp.async) while the page rows are
-//     looked up; then warp 9, from one lane,
-//     streams K and V through a two-stage ring with TMA: one 3-D box
+//   * warp 9 finds each item (a warp-wide prefix count over the requests),
+//     derives its key tiles and hands it to the other roles through a
+//     two-slot ring in shared memory (so that their loops carry no per-item
+//     arithmetic); it loads the Q tiles with TMA (box {64 dims, G heads,
+//     128/G tokens}) into three rotating buffers - a buffer is released by
+//     the epilogue that staged its tile's output through it, so the next
+//     item's first tile is loaded while the current item still computes -
+//     looks up page rows 32 page slots at a time with its lanes, a batch
+//     ahead, and from one lane streams K and V through a
+//     two-stage ring with TMA: one 3-D box
 //     {64 dims, 1 head, ps rows} per page and 64-dim block of D, 128-byte swizzle,
 //     completion counted on "full" mbarriers, slots returned on "empty" ones;
 //   * warp 8 (one lane) issues tcgen05.mma: S_i = Q_i K^T into TMEM columns
@@ -26,8 +34,9 @@
 //     that straddle a window or causal edge, and keeps a lazily rescaled
 //     running maximum (O in TMEM is rescaled only when the maximum grew by more
 //     than 2^8), writes P as packed bf16 pairs back to TMEM and signals the
-//     MMA lane; after the last tile it normalises O (with the sink) and stores
-//     its output row.
+//     MMA lane; after the item's last tile it normalises O (with the sink) and
+//     stores its output row, while the tensor core already computes the next
+//     item's first S.
 // KV pools are zero-initialised by the caller (as the pages' pools are), so
 // rows of a loaded page outside the query's key range hold finite values and
 // their zero softmax weight cancels them exactly; page slots of a key tile
@@ -56,10 +65,10 @@ constexpr int kBlock = kRows * 64 * 2;       // one 64-column block of a 128-row
 template <int D>
 struct Geo {
   static constexpr int kTileBytes = kRows * D * 2;
-  static constexpr int kOffQ = 0;                  // Q0, Q1
-  static constexpr int kOffK = 2 * kTileBytes;     // K stage 0, 1
-  static constexpr int kOffV = 4 * kTileBytes;     // V stage 0, 1
-  static constexpr int kOffRows = 6 * kTileBytes;  // int32 page rows [max_pages]
+  static constexpr int kOffQ = 0;                  // Q buffers 0, 1, 2
+  static constexpr int kOffK = 3 * kTileBytes;     // K stage 0, 1
+  static constexpr int kOffV = 5 * kTileBytes;     // V stage 0, 1
+  static constexpr int kOffBars = 7 * kTileBytes;  // mbarriers
   static constexpr int kCPR = D / 8;               // 16-byte chunks of a row
 };
 constexpr uint32_t kTmemCols = 512;
@@ -82,17 +91,12 @@ struct TcParams {
   const float *sinks;
   float scale_log2;
   __nv_bfloat16 *out;
-  int max_pages;
   int32_t *err;
 };
 
 // ------------------------------------------------------------------ PTX ---
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool pred) {
-  int sz = pred ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(sz));
 }
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
@@ -155,6 +159,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
+}
+
+// Pulls a box of the tensor into L2 (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
 }
 
 // tcgen05 shared-memory matrix descriptor: start >> 4 at [0,14), leading byte
@@ -248,42 +260,123 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 }
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
-// (row r, 16-byte chunk c in 0..15) of a 128 x 128 bf16 tile stored as two
-// 64-column blocks of [128 rows][128 B] with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t tile_off(int r, int c) {
-  return (uint32_t)((c >> 3) * kBlock + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
-
 __device__ __forceinline__ int64_t key_lo(int kind, int window, int64_t p) {
   if (kind == SWA_LAYER_FULL) return 0;
   if (kind == SWA_LAYER_SLIDING) return p - window > 0 ? p - window : 0;
   return (p / window) * window;
 }
 
-// Shared memory (offsets from a 1024-byte aligned base): Geo<D>.
+// Shared memory (offsets from a 1024-byte aligned base): Geo<D>, then the
+// mbarriers.  FULLQ / QFREE belong to the three Q buffers, IFULL / IEMPTY to
+// the two-slot ring through which the producer hands items to the others.
 enum { B_FULLK = 0, B_EMPTYK = 2, B_FULLV = 4, B_EMPTYV = 6, B_SDONE = 8, B_PREADY = 10,
-       B_ODONE = 12, B_DRAIN = 13, B_COUNT = 14 };
+       B_ODONE = 12, B_FULLQ = 14, B_QFREE = 17, B_IFULL = 20, B_IEMPTY = 22, B_DRAIN = 24,
+       B_COUNT = 25 };
+constexpr int kItemReaders = 9;              // the 8 softmax warps and the MMA lane
+
+// A work item: 2T consecutive query tokens of request b (clipped to the end
+// of its chunk, qend), starting at token q0 and key position pfirst, with its
+// key tiles (filled in by the producer, item_geo); b < 0 marks the end of the
+// CTA's items.
+struct Item {
+  int b, n_tok, n_tiles;                // request; tokens; key tiles
+  int64_t q0, qend, pfirst, kt0;        // first key tile kt0 (128-aligned)
+};
+struct ItemGeo {
+  int64_t n_tok, k_lo, k_hi, kt0;   // tokens; key range; first key tile (128-aligned)
+  int n_tiles;
+};
+__device__ __forceinline__ ItemGeo item_geo(const TcParams &P, const Item &it, int T2) {
+  ItemGeo g;
+  g.n_tok = min((int64_t)T2, it.qend - it.q0);
+  g.k_lo = key_lo(P.kind, P.window, it.pfirst);
+  g.k_hi = it.pfirst + g.n_tok - 1;
+  g.kt0 = (g.k_lo / kKeys) * kKeys;
+  g.n_tiles = (int)((g.k_hi - g.kt0) / kKeys + 1);
+  return g;
+}
+
+// Warp-collective: the item numbered tau (the latest tokens first) as a
+// request and its first token, or false past the last item.  The lanes take
+// 32 requests at a time and count their items with a prefix sum.
+__device__ __forceinline__ bool find_item(const TcParams &P, int64_t tau, int T2, int lane,
+                                          Item &it) {
+  int64_t acc = 0;
+  for (int b0 = 0; b0 < P.bs; b0 += 32) {
+    const int bb = b0 + lane;
+    int64_t lo = 0, hi = 0, n = 0;
+    if (bb < P.bs) {
+      lo = P.qo_indptr[bb];
+      hi = P.qo_indptr[bb + 1];
+      n = (hi - lo + T2 - 1) / T2;
+    }
+    int64_t incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, bb < P.bs && tau < acc + incl);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      const int64_t local = (tau - acc - __shfl_sync(0xffffffffu, incl - n, l)) * T2;
+      it.b = b0 + l;
+      it.q0 = __shfl_sync(0xffffffffu, lo, l) + local;
+      it.qend = __shfl_sync(0xffffffffu, hi, l);
+      it.pfirst = P.pre[it.b] + local;
+      return true;
+    }
+    acc += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return false;
+}
+
+// The page that holds key position pos of a request, in two steps so that
+// the load's latency can overlap other work: page_record() loads its record -
+// the request's req_to_token entry (full layers: rt_row) or its entry in the
+// request's SWA plan (hdr = the plan header h0, h2, h3, pages = the page list)
+// - or -1 when the plan holds none; page_first_row() turns a record into the
+// page's first row in the layer's K/V view, with the range and evicted-slot
+// checks (an offending page reads as page 0).
+__device__ __forceinline__ int32_t page_record(bool full, int ps_shift, const int32_t *rt_row,
+                                               int64_t h0, int64_t h2, int64_t h3,
+                                               const int32_t *pages, int64_t pos) {
+  if (full) return rt_row[pos];
+  const int64_t k = (pos >> ps_shift) - h2;
+  return (pos >= h0 && k >= 0 && k < h3) ? pages[k] : -1;
+}
+__device__ __forceinline__ int32_t page_first_row(bool full, int ps_shift, int64_t page_stride,
+                                                  int64_t max_page, int32_t rec, int32_t *err) {
+  int64_t page = full ? (rec >= 0 ? rec >> ps_shift : -1) : rec;
+  if (!full && page == 0) set_error(err, SWA_DEVERR_WINDOW_EVICTED);
+  if (page < 0 || page > max_page) {
+    set_error(err, SWA_DEVERR_RANGE);
+    page = 0;
+  }
+  return (int32_t)(page * page_stride);
+}
 
 template <int kD>
 __global__ void __launch_bounds__(kThreads, 1)
     k_extend_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                TcParams P) {
+                const __grid_constant__ CUtensorMap tmQ, TcParams P) {
   using Gm = Geo<kD>;
   constexpr int kTileBytes = Gm::kTileBytes, kOffQ = Gm::kOffQ, kOffK = Gm::kOffK;
-  constexpr int kOffV = Gm::kOffV, kOffRows = Gm::kOffRows, kCPR = Gm::kCPR;
+  constexpr int kOffV = Gm::kOffV, kCPR = Gm::kCPR;
   extern __shared__ char smem_raw[];
   char *smem = reinterpret_cast<char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(smem);
-  int32_t *s_rows = reinterpret_cast<int32_t *>(smem + kOffRows);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffRows + ((P.max_pages * 4 + 7) & ~7));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Gm::kOffBars);
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  __shared__ int64_t s_q0, s_qend, s_pfirst, s_req;
+  __shared__ Item s_item[2];
+  __shared__ int32_t s_rows[2][32];        // page rows of 32 page slots, double-buffered
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kvh = blockIdx.y;
   const int G = P.G;
   const int T = kRows / G;                 // tokens per Q tile
+  const int T2 = 2 * T;                    // tokens per item
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   // ---- once per CTA: TMEM, barriers ----
@@ -302,8 +395,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_EMPTYV + i), 1);
       mbar_init(bar(B_SDONE + i), 1);
       mbar_init(bar(B_PREADY + i), kRows);
+      mbar_init(bar(B_ODONE + i), 1);
+      mbar_init(bar(B_IFULL + i), 1);
+      mbar_init(bar(B_IEMPTY + i), kItemReaders);
     }
-    mbar_init(bar(B_ODONE), 1);
+    for (int j = 0; j < 3; ++j) {
+      mbar_init(bar(B_FULLQ + j), 1);
+      mbar_init(bar(B_QFREE + j), kRows);
+    }
     mbar_init(bar(B_DRAIN), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -313,138 +412,165 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kIdS = idesc_f16(128, 128, false);
   constexpr uint32_t kIdO = idesc_f16(128, kD, true);
 
-  // Persistent: the CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...
-  // Every barrier phase follows the CTA's running tile count tg0 (key tiles
-  // of its earlier items) or item count n_done, so the rings run on across
-  // items; each item ends with all roles joined (its Q tiles and TMEM free).
-  int tg0 = 0, n_done = 0;
-  // Producer only: running tile counts whose K / V loads were issued (tile T
-  // arms phase T >> 1 of "full" barrier T & 1), so that an abort can wait for
-  // the loads still in flight.
-  int k_issued = 0, v_issued = 0;
-  for (int item = blockIdx.x; item < P.items_upper; item += gridDim.x) {
-  __syncthreads();   // every thread has read the previous item's fields
-  // ---- work item: two Q tiles of one request, latest first ----
-  if (tid == 0) {
-    int64_t tau = (int64_t)P.items_upper - 1 - item, acc = 0;
-    s_req = -1;
-    for (int b = 0; b < P.bs; ++b) {
-      const int64_t ext = P.qo_indptr[b + 1] - P.qo_indptr[b];
-      const int64_t n = (ext + 2 * T - 1) / (2 * T);
-      if (tau < acc + n) {
-        const int64_t local = (tau - acc) * 2 * T;
-        s_req = b;
-        s_q0 = P.qo_indptr[b] + local;
-        s_qend = P.qo_indptr[b + 1];
-        s_pfirst = P.pre[b] + local;
-        break;
-      }
-      acc += n;
-    }
-  }
-  __syncthreads();
-  if (s_req < 0) continue;
-  const int b = (int)s_req;
-  const int64_t q0 = s_q0, n_tok = min((int64_t)2 * T, s_qend - s_q0);
-  const int64_t p_first = s_pfirst, p_last = p_first + n_tok - 1;
-  const int64_t k_lo = key_lo(P.kind, P.window, p_first);
-  const int64_t k_hi = p_last;
-  const int64_t kt0 = (k_lo / kKeys) * kKeys;      // key tiles are 128-aligned
-  const int n_tiles = (int)((k_hi - kt0) / kKeys + 1);
-  const int64_t pg0 = kt0 / P.ps;
-  const int n_pg = (int)(k_hi / P.ps - pg0 + 1);
-  if (n_pg > P.max_pages || n_tiles * (kKeys / P.ps) > P.max_pages) {
-    if (tid == 0) set_error(P.err, SWA_DEVERR_RANGE);
-    continue;
-  }
-
-  // Q rows of both tiles, gathered by every thread (cp.async, zero fill past
-  // the chunk); their latency overlaps the page-row lookups below.
-  {
-    const int Hq = P.hkv * G;
-    for (int i = tid; i < 2 * kRows * kCPR; i += kThreads) {
-      const int qt = i / (kRows * kCPR), rr = (i / kCPR) % kRows, c = i % kCPR;
-      const int64_t tok = q0 + qt * T + rr / G;
-      const bool ok = tok < s_qend && (qt * T + rr / G) < n_tok;
-      const __nv_bfloat16 *src = P.q + ((ok ? tok : q0) * Hq + kvh * G + rr % G) * kD + c * 8;
-      cp_async16(sb + kOffQ + qt * kTileBytes + tile_off(rr, c), src, ok);
-    }
-  }
-  const int64_t max_page = P.pool_rows / P.ps - 1;
-  // Every page slot of every key tile is loaded, so the stage buffers never
-  // hold uninitialised bytes and need no clearing: slots outside the key
-  // range (-1 here) load the item's first in-range page instead, whose
-  // values are finite and get zero weight.  (Not page 0: mapping 0 marks an
-  // evicted SWA slot, which attention must never read.)
-  const int n_slots = n_tiles * (kKeys / P.ps);
-  for (int i = tid; i < n_slots; i += kThreads) {
-    const int64_t pos0 = (pg0 + i) * P.ps;
-    const int64_t pos = pos0 > k_lo ? pos0 : k_lo;
-    int64_t page = -2;                       // -2: outside the key range
-    if (i < n_pg && pos <= k_hi && pos0 + P.ps > k_lo) {
-      if (P.kind == SWA_LAYER_FULL) {
-        page = P.rt[P.req_idx[b] * P.rt_stride + pos] / P.ps;
-      } else {
-        const int32_t *h = P.plan.hdr + b * 4;
-        const int64_t k = pos / P.ps - h[2];
-        page = (pos >= h[0] && k >= 0 && k < h[3]) ? P.plan.pages[(int64_t)b * P.plan.max_pages + k]
-                                                   : -1;
-        if (page == 0) set_error(P.err, SWA_DEVERR_WINDOW_EVICTED);
-      }
-      if (page < 0 || page > max_page) {
-        set_error(P.err, SWA_DEVERR_RANGE);
-        page = 0;
-      }
-    }
-    s_rows[i] = page == -2 ? -1 : (int32_t)(page * P.page_stride);
-  }
-  const int slot_lo = (int)(k_lo / P.ps - pg0);   // first in-range slot
-  asm volatile("cp.async.wait_all;\n" ::: "memory");
-  fence_async_smem();   // Q (written by cp.async) is read by the tensor core
-  __syncthreads();
-  tc_fence_after();
+  // Persistent: the producer takes items blockIdx.x, blockIdx.x + gridDim.x,
+  // ... and publishes each one; the other roles follow the published order.
+  // Every barrier phase follows a running count - key tiles (tg), items (nd)
+  // or Q tiles (u = 2 nd + tile, buffer u % 3) - so the rings run on across
+  // items and no role waits for another at an item boundary.
+  // Producer only, for the abort path: running counts of the K / V tiles and
+  // Q tiles whose loads were issued.
+  int k_issued = 0, v_issued = 0, q_issued = 0;
 
   if (warp == 9) {
-    // ===================== producer: K/V pages =====================
-    if (lane == 0) {
-      const int pages_per_tile = kKeys / P.ps;
-      for (int t = 0; t < n_tiles && !s_abort; ++t) {
-        const int T = tg0 + t;             // the CTA's running tile count
-        const int s = T & 1;
-        for (int kv = 0; kv < 2; ++kv) {
-          if (T >= 2 && !mbar_wait(bar((kv ? B_EMPTYV : B_EMPTYK) + s), ((T >> 1) - 1) & 1, &s_abort))
-            break;
-          const uint32_t full = bar((kv ? B_FULLV : B_FULLK) + s);
-          mbar_expect_tx(full, (uint32_t)kTileBytes);   // every page slot is loaded
-          if (kv) v_issued = T + 1;
-          else k_issued = T + 1;
-          const uint32_t dst = sb + (kv ? kOffV : kOffK) + s * kTileBytes;
-          for (int i = 0; i < pages_per_tile; ++i) {
-            const int pi = t * pages_per_tile + i;
-            const int32_t row = s_rows[pi] >= 0 ? s_rows[pi] : s_rows[slot_lo];
-            for (int h = 0; h < kD / 64; ++h)
-              tma_load_3d(dst + h * kBlock + i * P.ps * 128, kv ? &tmV : &tmK, h * 64, kvh, row, full);
+    // ===================== producer: items, Q tiles, K/V pages =====================
+    const int64_t max_page = P.pool_rows / P.ps - 1;
+    const int ppt = kKeys / P.ps;            // pages per key tile (at most 8)
+    int n_pub = 0, tg = 0;
+    bool ok = true;
+    auto wait_all = [&](uint32_t b, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(b, parity, &s_abort));
+    };
+    // Item n goes to ring slot n & 1 once its readers have copied item n - 2.
+    auto publish = [&](const Item &it) {
+      const int slot = n_pub & 1;
+      if (n_pub >= 2 && !wait_all(bar(B_IEMPTY + slot), ((n_pub >> 1) - 1) & 1)) return false;
+      if (lane == 0) {
+        s_item[slot] = it;
+        mbar_arrive(bar(B_IFULL + slot));
+      }
+      __syncwarp();
+      ++n_pub;
+      return true;
+    };
+    // Q tile u of the CTA (tokens from tok on) into buffer u % 3, once the
+    // epilogue of the tile that used the buffer before has released it.
+    auto load_q = [&](int u, int64_t tok) {
+      const int j = u % 3, f = u / 3;
+      if (f >= 1 && !wait_all(bar(B_QFREE + j), (f - 1) & 1)) return false;
+      if (lane == 0) {
+        mbar_expect_tx(bar(B_FULLQ + j), (uint32_t)kTileBytes);
+        for (int h = 0; h < kD / 64; ++h)
+          tma_load_3d(sb + kOffQ + j * kTileBytes + h * kBlock, &tmQ, h * 64, kvh * G, (int)tok,
+                      bar(B_FULLQ + j));
+      }
+      __syncwarp();
+      q_issued = u + 1;
+      return true;
+    };
+    for (int item = blockIdx.x; ok && item < P.items_upper; item += gridDim.x) {
+      Item it;
+      if (!find_item(P, (int64_t)P.items_upper - 1 - item, T2, lane, it)) continue;
+      const ItemGeo g = item_geo(P, it, T2);
+      it.n_tok = (int)g.n_tok;
+      it.n_tiles = g.n_tiles;
+      it.kt0 = g.kt0;
+      if (!(ok = publish(it))) break;
+      const int64_t pg0 = g.kt0 >> P.ps_shift;
+      const int n_pg = (int)((g.k_hi >> P.ps_shift) - pg0 + 1);
+      const int n_slots = g.n_tiles * ppt;
+      const bool full_layer = P.kind == SWA_LAYER_FULL;
+      const int32_t *rt_row = full_layer ? P.rt + P.req_idx[it.b] * P.rt_stride : nullptr;
+      const int32_t *pages = full_layer ? nullptr : P.plan.pages + (int64_t)it.b * P.plan.max_pages;
+      int64_t h0 = 0, h2 = 0, h3 = 0;
+      if (!full_layer) {
+        const int32_t *hdr = P.plan.hdr + it.b * 4;
+        h0 = hdr[0];
+        h2 = hdr[2];
+        h3 = hdr[3];
+      }
+      auto first_row = [&](int32_t rec) {
+        return page_first_row(full_layer, P.ps_shift, P.page_stride, max_page, rec, P.err);
+      };
+      // Every page slot of every key tile is loaded, so the stage buffers never
+      // hold uninitialised bytes and need no clearing: slots outside the key
+      // range load the item's first in-range page instead, whose values are
+      // finite and get zero weight.  (Not page 0: mapping 0 marks an evicted
+      // SWA slot, which attention must never read.)
+      const int32_t row_lo =
+          first_row(page_record(full_layer, P.ps_shift, rt_row, h0, h2, h3, pages, g.k_lo));
+      // Records of the 32 page slots 32 k .. 32 k + 31, lane i for slot 32 k + i
+      // (in range: -2 marks a slot outside the key range).
+      auto batch_records = [&](int k) {
+        const int i = 32 * k + lane;
+        const int64_t pos0 = (pg0 + i) << P.ps_shift;
+        const int64_t pos = pos0 > g.k_lo ? pos0 : g.k_lo;
+        return i < n_pg && pos <= g.k_hi && pos0 + P.ps > g.k_lo
+                   ? page_record(full_layer, P.ps_shift, rt_row, h0, h2, h3, pages, pos)
+                   : -2;
+      };
+      auto batch_rows = [&](int32_t rec) { return rec == -2 ? row_lo : first_row(rec); };
+      // Rows of the item's first 32 slots go to s_rows[0]; the records of the
+      // next 32 are loaded now and turned into rows a batch later, so that a
+      // batch's lookups overlap the previous batch's 32 / ppt tiles.
+      s_rows[0][lane] = batch_rows(batch_records(0));
+      int32_t rec_next = n_slots > 32 ? batch_records(1) : -2;
+      __syncwarp();
+      const int u0 = 2 * (n_pub - 1);
+      if (!(ok = load_q(u0, it.q0))) break;
+      // The second tile's buffer is released later (by the previous item's
+      // first epilogue); its rows are pulled into L2 meanwhile.
+      if (lane == 0 && it.q0 + T < it.qend)
+        for (int h = 0; h < kD / 64; ++h) tma_prefetch_3d(&tmQ, h * 64, kvh * G, (int)(it.q0 + T));
+      for (int t = 0; t < g.n_tiles && ok; ++t) {
+        const int Tr = tg + t;               // the CTA's running tile count
+        const int s = Tr & 1;
+        const int i0 = t * ppt;              // the tile's first page slot (ppt divides 32)
+        if (i0 > 0 && (i0 & 31) == 0) {
+          s_rows[(i0 >> 5) & 1][lane] = batch_rows(rec_next);
+          rec_next = i0 + 32 < n_slots ? batch_records((i0 >> 5) + 1) : -2;
+          __syncwarp();
+        }
+        // One lane waits for the stages and issues the loads.
+        int good = 1;
+        if (lane == 0) {
+          const int32_t *rows = &s_rows[(i0 >> 5) & 1][i0 & 31];
+          for (int kv = 0; kv < 2 && good; ++kv) {
+            if (Tr >= 2 &&
+                !(good = mbar_wait(bar((kv ? B_EMPTYV : B_EMPTYK) + s), ((Tr >> 1) - 1) & 1,
+                                   &s_abort)))
+              break;
+            const uint32_t full = bar((kv ? B_FULLV : B_FULLK) + s);
+            const uint32_t dst = sb + (kv ? kOffV : kOffK) + s * kTileBytes;
+            mbar_expect_tx(full, (uint32_t)kTileBytes);
+            for (int i = 0; i < ppt; ++i)
+              for (int h = 0; h < kD / 64; ++h)
+                tma_load_3d(dst + h * kBlock + i * P.ps * 128, kv ? &tmV : &tmK, h * 64, kvh,
+                            rows[i], full);
+            if (kv) v_issued = Tr + 1;
+            else k_issued = Tr + 1;
           }
         }
+        ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+        if (ok && t == 0) ok = load_q(u0 + 1, it.q0 + T);
+        __syncwarp();
       }
+      tg += g.n_tiles;
+    }
+    if (ok) {
+      Item end;
+      end.b = -1;
+      end.n_tok = end.n_tiles = 0;
+      end.q0 = end.qend = end.pfirst = end.kt0 = 0;
+      publish(end);
     }
   } else if (warp == 8) {
     // ===================== MMA issue (one lane) =====================
     // Order per tile t: O0(t), S0(t+1), O1(t), S1(t+1) - softmax group 0 works
     // on tile t+1 while the tensor core runs O1(t) and S1(t+1), and group 1
-    // likewise one slot later.
-    // Shared-memory descriptors built once per tile and stage: a K step only
+    // likewise one slot later.  An item's first S0 is issued as soon as its Q
+    // tile and first K tile have landed, while the groups still drain the
+    // previous item's O.
+    // Shared-memory descriptors built once per buffer and stage: a K step only
     // advances the 14-bit address field by (byte offset >> 4), which cannot
     // carry out of the field (shared addresses stay below 256 KB), so each
     // product's descriptors are one add from these.
-    const uint64_t dq0 = smem_desc(sb + kOffQ, 16, 1024);
-    const uint64_t dq1 = smem_desc(sb + kOffQ + kTileBytes, 16, 1024);
+    const uint64_t dq0 = smem_desc(sb + kOffQ, 16, 1024);   // buffer j: + j * kTileBytes >> 4
     const uint64_t dk0 = smem_desc(sb + kOffK, 16, 1024);
     const uint64_t dk1 = smem_desc(sb + kOffK + kTileBytes, 16, 1024);
     const uint64_t dv0 = smem_desc(sb + kOffV, kBlock, 1024);
     const uint64_t dv1 = smem_desc(sb + kOffV + kTileBytes, kBlock, 1024);
-    auto issue_s = [&](int i, int T) {     // T: running tile count (stage)
-      const uint64_t qd = i ? dq1 : dq0, kd = (T & 1) ? dk1 : dk0;
+    auto issue_s = [&](int i, uint64_t qd, int Tr) {   // Tr: running tile count (stage)
+      const uint64_t kd = (Tr & 1) ? dk1 : dk0;
 #pragma unroll
       for (int ks = 0; ks < kD / 16; ++ks) {
         const uint64_t off16 = ((ks >> 2) * kBlock + (ks & 3) * 32) >> 4;
@@ -452,178 +578,210 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_commit(bar(B_SDONE + i));
     };
-    auto issue_o = [&](int i, int t, int T) {   // t: tile of the item, T: running count
-      const uint64_t vd = (T & 1) ? dv1 : dv0;
+    auto issue_o = [&](int i, int t, int Tr) {   // t: tile of the item, Tr: running count
+      const uint64_t vd = (Tr & 1) ? dv1 : dv0;
 #pragma unroll
       for (int ks = 0; ks < kKeys / 16; ++ks)
         mma_ts(tmem + 256 + i * kD, tmem + i * 128 + ks * 8, vd + (uint64_t)(ks * 16 * 128 >> 4),
                kIdO, (t > 0 || ks > 0) ? 1u : 0u);
     };
-    if (lane == 0 && mbar_wait(bar(B_FULLK + (tg0 & 1)), (tg0 >> 1) & 1, &s_abort)) {
-      tc_fence_after();
-      issue_s(0, tg0);
-      issue_s(1, tg0);
-      tc_commit(bar(B_EMPTYK + (tg0 & 1)));
-      for (int t = 0; t < n_tiles; ++t) {
-        const int T = tg0 + t;
-        const int s = T & 1, s1 = (T + 1) & 1;
-        const bool more = t + 1 < n_tiles;
-        if (!mbar_wait(bar(B_FULLV + s), (T >> 1) & 1, &s_abort)) break;
-        if (!mbar_wait(bar(B_PREADY + 0), T & 1, &s_abort)) break;
+    if (lane == 0) {
+      int tg = 0, nd = 0;
+      for (bool ok = true; ok;) {
+        const int slot = nd & 1;
+        if (!mbar_wait(bar(B_IFULL + slot), (nd >> 1) & 1, &s_abort)) break;
+        const Item it = s_item[slot];
+        mbar_arrive(bar(B_IEMPTY + slot));
+        if (it.b < 0) break;
+        const int n_tiles = it.n_tiles;
+        const int u0 = 2 * nd;
+        const uint64_t qa = dq0 + (uint64_t)((u0 % 3) * kTileBytes >> 4);
+        const uint64_t qb = dq0 + (uint64_t)(((u0 + 1) % 3) * kTileBytes >> 4);
+        if (!mbar_wait(bar(B_FULLK + (tg & 1)), (tg >> 1) & 1, &s_abort)) break;
+        if (!mbar_wait(bar(B_FULLQ + u0 % 3), (u0 / 3) & 1, &s_abort)) break;
         tc_fence_after();
-        issue_o(0, t, T);
-        if (more) {
-          if (!mbar_wait(bar(B_FULLK + s1), ((T + 1) >> 1) & 1, &s_abort)) break;
+        issue_s(0, qa, tg);
+        if (!mbar_wait(bar(B_FULLQ + (u0 + 1) % 3), ((u0 + 1) / 3) & 1, &s_abort)) break;
+        tc_fence_after();
+        issue_s(1, qb, tg);
+        tc_commit(bar(B_EMPTYK + (tg & 1)));
+        for (int t = 0; t < n_tiles; ++t) {
+          const int Tr = tg + t;
+          const int s = Tr & 1, s1 = (Tr + 1) & 1;
+          const bool more = t + 1 < n_tiles;
+          if (!(ok = mbar_wait(bar(B_FULLV + s), (Tr >> 1) & 1, &s_abort))) break;
+          if (!(ok = mbar_wait(bar(B_PREADY + 0), Tr & 1, &s_abort))) break;
           tc_fence_after();
-          issue_s(0, T + 1);
+          issue_o(0, t, Tr);
+          if (more) {
+            if (!(ok = mbar_wait(bar(B_FULLK + s1), ((Tr + 1) >> 1) & 1, &s_abort))) break;
+            tc_fence_after();
+            issue_s(0, qa, Tr + 1);
+          } else {
+            tc_commit(bar(B_ODONE + 0));
+          }
+          if (!(ok = mbar_wait(bar(B_PREADY + 1), Tr & 1, &s_abort))) break;
+          tc_fence_after();
+          issue_o(1, t, Tr);
+          tc_commit(bar(B_EMPTYV + s));
+          if (more) {
+            issue_s(1, qb, Tr + 1);
+            tc_commit(bar(B_EMPTYK + s1));
+          } else {
+            tc_commit(bar(B_ODONE + 1));
+          }
         }
-        if (!mbar_wait(bar(B_PREADY + 1), T & 1, &s_abort)) break;
-        tc_fence_after();
-        issue_o(1, t, T);
-        tc_commit(bar(B_EMPTYV + s));
-        if (more) {
-          issue_s(1, T + 1);
-          tc_commit(bar(B_EMPTYK + s1));
-        }
+        tg += n_tiles;
+        ++nd;
       }
     }
-    if (lane == 0) tc_commit(bar(B_ODONE));
   } else {
     // ===================== softmax group i (warps 4i .. 4i+3) =====================
     const int grp = warp >> 2;
     const int r = tid & 127;                    // row of Q tile grp = TMEM lane
     const int tr = grp * T + r / G, g = r % G;  // token offset in the item, head
-    const bool row_valid = tr < n_tok;
-    const int64_t p_row = p_first + tr;
-    const int64_t lo_row = key_lo(P.kind, P.window, p_row);
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + grp * 128 + lane_off;
     const uint32_t tO = tmem + 256 + grp * kD + lane_off;
-    float m_run = -INFINITY, l_run = 0.f;
-    bool alive = true;
-    for (int t = 0; t < n_tiles; ++t) {
-      // Warp-uniform outcome: the TMEM loads below are warp-collective.
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_SDONE + grp), (tg0 + t) & 1, &s_abort))) {
-        alive = false;
+    const int Hq = P.hkv * G;
+    int tg = 0, nd = 0;
+    for (;;) {
+      const int slot = nd & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_IFULL + slot), (nd >> 1) & 1, &s_abort)))
         break;
-      }
-      tc_fence_after();
-      const int64_t j0 = kt0 + (int64_t)t * kKeys;
-      const bool edge = !row_valid || j0 < lo_row || j0 + kKeys - 1 > p_row;
-      // Key e of this tile counts iff lo_row <= j0 + e <= p_row (edge tiles only).
-      const int e_lo = edge ? (int)max((int64_t)0, min((int64_t)kKeys, lo_row - j0)) : 0;
-      const int e_hi = edge ? (row_valid ? (int)max((int64_t)-1, min((int64_t)kKeys - 1, p_row - j0))
-                                         : -1)
-                            : kKeys - 1;
-      // Interior tiles (no row of the warp at a window or causal edge) skip
-      // the per-key masks entirely.
-      const bool masked = __any_sync(0xffffffffu, edge);
-      // Keys outside this row's range read as -inf (edge tiles only): the
-      // max and the exponentials below then need no per-key test.
-      auto mask_in_place = [&](uint32_t (&rr)[64], int cb) {
-#pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          const int ee = cb * 64 + e;
-          if (ee < e_lo || ee > e_hi) rr[e] = 0xff800000u;   // -inf
+      const Item it = s_item[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_IEMPTY + slot));
+      if (it.b < 0) break;
+      const bool row_valid = tr < it.n_tok;
+      const int64_t p_row = it.pfirst + tr;
+      const int64_t lo_row = key_lo(P.kind, P.window, p_row);
+      float m_run = -INFINITY, l_run = 0.f;
+      bool alive = true;
+      for (int t = 0; t < it.n_tiles; ++t) {
+        // Warp-uniform outcome: the TMEM loads below are warp-collective.
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_SDONE + grp), (tg + t) & 1, &s_abort))) {
+          alive = false;
+          break;
         }
-      };
-      // One pass over S, 64 keys at a time: each chunk's maximum is checked
-      // against the running reference maximum m_run, which moves only when a
-      // chunk exceeds it by more than kRescaleGap (weights stay below
-      // 2^kRescaleGap meanwhile).  A move rescales what was accumulated
-      // against the old reference - O of earlier tiles, the running sum and,
-      // for the second chunk, the first chunk's P already in TMEM - before
-      // this chunk's exponentials.  The 64-key loops stay rolled: one copy of
-      // each body keeps the softmax code inside the instruction cache.
-      const float sc = P.scale_log2;
-      const uint64_t sc2 = f2pack(sc, sc);
-      uint64_t acc2[2] = {0ull, 0ull};   // running pair sums (two chains)
-#pragma unroll 1
-      for (int cb = 0; cb < 2; ++cb) {
-        uint32_t rr[64];
-        TC_LD32(tS + cb * 64, rr);        // two loads in flight before one wait
-        TC_LD32(tS + cb * 64 + 32, (rr + 32));
-        tc_wait_ld();
-        if (masked) mask_in_place(rr, cb);
-        // four independent chains of three-input maxima
-        float m2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int e = 0; e < 64; e += 2)
-          m2[(e >> 1) & 3] = max3(m2[(e >> 1) & 3], __uint_as_float(rr[e]), __uint_as_float(rr[e + 1]));
-        float cm = max3(m2[0], m2[1], fmaxf(m2[2], m2[3]));
-        cm = cm == -INFINITY ? -INFINITY : cm * sc;
-        // A row whose maximum is still -inf has accumulated exactly nothing
-        // (every P so far was 0), so its first finite maximum needs no
-        // rescale (factor 1): only moves of a finite maximum pay for one.
-        float corr = 1.f;
-        if (cm > m_run + kRescaleGap || (m_run == -INFINITY && cm != -INFINITY)) {
-          corr = m_run == -INFINITY ? 1.f : exp2f(m_run - cm);
-          m_run = cm;
-        }
-        if (__any_sync(0xffffffffu, corr != 1.f)) {
-          if (t > 0) {
-#pragma unroll 1
-            for (int ob = 0; ob < kD / 32; ++ob) {
-              uint32_t ro[32];
-              TC_LD32(tO + ob * 32, ro);
+        tc_fence_after();
+        const int64_t j0 = it.kt0 + (int64_t)t * kKeys;
+        const bool edge = !row_valid || j0 < lo_row || j0 + kKeys - 1 > p_row;
+        // Key e of this tile counts iff lo_row <= j0 + e <= p_row (edge tiles only).
+        const int e_lo = edge ? (int)max((int64_t)0, min((int64_t)kKeys, lo_row - j0)) : 0;
+        const int e_hi = edge ? (row_valid ? (int)max((int64_t)-1, min((int64_t)kKeys - 1, p_row - j0))
+                                           : -1)
+                              : kKeys - 1;
+        // Interior tiles (no row of the warp at a window or causal edge) skip
+        // the per-key masks entirely.
+        const bool masked = __any_sync(0xffffffffu, edge);
+        // Keys outside this row's range read as -inf (edge tiles only): the
+        // max and the exponentials below then need no per-key test.
+        auto mask_in_place = [&](uint32_t (&rr)[64], int cb) {
+  #pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            const int ee = cb * 64 + e;
+            if (ee < e_lo || ee > e_hi) rr[e] = 0xff800000u;   // -inf
+          }
+        };
+        // One pass over S, 64 keys at a time: each chunk's maximum is checked
+        // against the running reference maximum m_run, which moves only when a
+        // chunk exceeds it by more than kRescaleGap (weights stay below
+        // 2^kRescaleGap meanwhile).  A move rescales what was accumulated
+        // against the old reference - O of earlier tiles, the running sum and,
+        // for the second chunk, the first chunk's P already in TMEM - before
+        // this chunk's exponentials.  The 64-key loops stay rolled: one copy of
+        // each body keeps the softmax code inside the instruction cache.
+        const float sc = P.scale_log2;
+        const uint64_t sc2 = f2pack(sc, sc);
+        uint64_t acc2[2] = {0ull, 0ull};   // running pair sums (two chains)
+  #pragma unroll 1
+        for (int cb = 0; cb < 2; ++cb) {
+          uint32_t rr[64];
+          TC_LD32(tS + cb * 64, rr);        // two loads in flight before one wait
+          TC_LD32(tS + cb * 64 + 32, (rr + 32));
+          tc_wait_ld();
+          if (masked) mask_in_place(rr, cb);
+          // four independent chains of three-input maxima
+          float m2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  #pragma unroll
+          for (int e = 0; e < 64; e += 2)
+            m2[(e >> 1) & 3] = max3(m2[(e >> 1) & 3], __uint_as_float(rr[e]), __uint_as_float(rr[e + 1]));
+          float cm = max3(m2[0], m2[1], fmaxf(m2[2], m2[3]));
+          cm = cm == -INFINITY ? -INFINITY : cm * sc;
+          // A row whose maximum is still -inf has accumulated exactly nothing
+          // (every P so far was 0), so its first finite maximum needs no
+          // rescale (factor 1): only moves of a finite maximum pay for one.
+          float corr = 1.f;
+          if (cm > m_run + kRescaleGap || (m_run == -INFINITY && cm != -INFINITY)) {
+            corr = m_run == -INFINITY ? 1.f : exp2f(m_run - cm);
+            m_run = cm;
+          }
+          if (__any_sync(0xffffffffu, corr != 1.f)) {
+            if (t > 0) {
+  #pragma unroll 1
+              for (int ob = 0; ob < kD / 32; ++ob) {
+                uint32_t ro[32];
+                TC_LD32(tO + ob * 32, ro);
+                tc_wait_ld();
+  #pragma unroll
+                for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * corr);
+                TC_ST32(tO + ob * 32, ro);
+              }
+            }
+            if (cb == 1) {
+              // the first chunk's P (32 columns of bf16 pairs) against the new reference
+              uint32_t pp[32];
+              tc_wait_st();
+              TC_LD32(tS, pp);
               tc_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * corr);
-              TC_ST32(tO + ob * 32, ro);
+  #pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&pp[e]);
+                const float2 f = __bfloat1622float2(h);
+                h = __floats2bfloat162_rn(f.x * corr, f.y * corr);
+                pp[e] = *reinterpret_cast<uint32_t *>(&h);
+              }
+              TC_ST32(tS, pp);
             }
+            float a0, a1, b0, b1;
+            f2unpack(acc2[0], a0, a1);
+            f2unpack(acc2[1], b0, b1);
+            acc2[0] = f2pack(a0 * corr, a1 * corr);
+            acc2[1] = f2pack(b0 * corr, b1 * corr);
+            l_run *= corr;
           }
-          if (cb == 1) {
-            // the first chunk's P (32 columns of bf16 pairs) against the new reference
-            uint32_t pp[32];
-            tc_wait_st();
-            TC_LD32(tS, pp);
-            tc_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&pp[e]);
-              const float2 f = __bfloat1622float2(h);
-              h = __floats2bfloat162_rn(f.x * corr, f.y * corr);
-              pp[e] = *reinterpret_cast<uint32_t *>(&h);
-            }
-            TC_ST32(tS, pp);
+          const float mu = m_run == -INFINITY ? 0.f : m_run;
+          const uint64_t nmu2 = f2pack(-mu, -mu);
+          // P = exp2(scale*s - m) as packed bf16 pairs, written over the S
+          // columns already consumed (64-key chunk cb -> columns [32 cb, 32 cb + 32)).
+          uint32_t pk[32];
+  #pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float t0, t1;
+            f2unpack(fma2(f2pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1])), sc2, nmu2),
+                     t0, t1);
+            const float a0 = ex2(t0);
+            const float a1 = ex2(t1);
+            acc2[e & 1] = add2(acc2[e & 1], f2pack(a0, a1));
+            __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
+            pk[e] = *reinterpret_cast<uint32_t *>(&h);
           }
-          float a0, a1, b0, b1;
-          f2unpack(acc2[0], a0, a1);
-          f2unpack(acc2[1], b0, b1);
-          acc2[0] = f2pack(a0 * corr, a1 * corr);
-          acc2[1] = f2pack(b0 * corr, b1 * corr);
-          l_run *= corr;
+          TC_ST32(tS + cb * 32, pk);
         }
-        const float mu = m_run == -INFINITY ? 0.f : m_run;
-        const uint64_t nmu2 = f2pack(-mu, -mu);
-        // P = exp2(scale*s - m) as packed bf16 pairs, written over the S
-        // columns already consumed (64-key chunk cb -> columns [32 cb, 32 cb + 32)).
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float t0, t1;
-          f2unpack(fma2(f2pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1])), sc2, nmu2),
-                   t0, t1);
-          const float a0 = ex2(t0);
-          const float a1 = ex2(t1);
-          acc2[e & 1] = add2(acc2[e & 1], f2pack(a0, a1));
-          __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
-          pk[e] = *reinterpret_cast<uint32_t *>(&h);
+        {
+          float s0, s1, s2, s3;
+          f2unpack(acc2[0], s0, s1);
+          f2unpack(acc2[1], s2, s3);
+          l_run += (s0 + s1) + (s2 + s3);
         }
-        TC_ST32(tS + cb * 32, pk);
+        tc_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(B_PREADY + grp));
       }
-      {
-        float s0, s1, s2, s3;
-        f2unpack(acc2[0], s0, s1);
-        f2unpack(acc2[1], s2, s3);
-        l_run += (s0 + s1) + (s2 + s3);
-      }
-      tc_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(B_PREADY + grp));
-    }
-    // ---- epilogue ----
-    if (alive && __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), n_done & 1, &s_abort))) {
+      if (!alive) break;
+      // ---- epilogue ----
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_ODONE + grp), nd & 1, &s_abort))) break;
       tc_fence_after();
       float sg2 = -INFINITY;
       if (P.sinks) sg2 = P.sinks[kvh * G + g] * 1.4426950408889634f;
@@ -632,11 +790,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float rsc = exp2f(mr - mfin);
       const float denom = l_run * rsc + (P.sinks ? exp2f(sg2 - mfin) : 0.f);
       const float f = denom > 0.f ? rsc / denom : 0.f;
-      const int Hq = P.hkv * G;
-      // The warp's 32 output rows go through shared memory (the Q tile area:
-      // every product that read it has completed by ODONE), so that the global
-      // stores are whole 256-byte rows written by 16 consecutive lanes.
-      char *stage = smem + kOffQ + grp * kTileBytes + (warp & 3) * 32 * (kD * 2);
+      // The warp's 32 output rows go through shared memory (this tile's Q
+      // buffer: every product that read it has completed by ODONE), so that
+      // the global stores are whole rows written by consecutive lanes.
+      const int jq = (2 * nd + grp) % 3;
+      char *stage = smem + kOffQ + jq * kTileBytes + (warp & 3) * 32 * (kD * 2);
 #pragma unroll 1
       for (int cb = 0; cb < kD / 64; ++cb) {
         uint32_t rr[64];
@@ -663,22 +821,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = idx / kCPR, c = idx % kCPR;
         const int rw = (warp & 3) * 32 + i;     // row of Q tile grp
         const int trw = grp * T + rw / G;
-        if (trw < n_tok) {
+        if (trw < it.n_tok) {
           const uint4 v =
               *reinterpret_cast<const uint4 *>(stage + i * (kD * 2) + ((c ^ (i & (kCPR - 1))) << 4));
-          *reinterpret_cast<uint4 *>(P.out + ((q0 + trw) * Hq + kvh * G + rw % G) * kD + c * 8) = v;
+          *reinterpret_cast<uint4 *>(P.out + ((it.q0 + trw) * Hq + kvh * G + rw % G) * kD + c * 8) =
+              v;
         }
       }
+      // The buffer's next contents arrive by TMA (the async proxy): order
+      // these accesses before it, then release the buffer.
+      fence_async_smem();
+      mbar_arrive(bar(B_QFREE + jq));
+      tg += it.n_tiles;
+      ++nd;
     }
   }
-  // end of the item: all roles joined before its Q tiles and TMEM are reused
-  tc_fence_before();
+  // Every role has left its loop: s_abort is final.
   __syncthreads();
-  tg0 += n_tiles;
-  ++n_done;
-  if (s_abort) break;
-  tc_fence_after();
-  }
   if (s_abort) {
     // A role gave up a wait.  Loads and products already issued complete on
     // their own; wait for them before the shared memory and TMEM they write
@@ -689,6 +848,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nk = (k_issued + 1 - i) >> 1, nv = (v_issued + 1 - i) >> 1;  // phases armed
         if (nk) mbar_drain(bar(B_FULLK + i), (nk - 1) & 1);
         if (nv) mbar_drain(bar(B_FULLV + i), (nv - 1) & 1);
+      }
+      for (int j = 0; j < 3; ++j) {
+        const int nf = q_issued > j ? (q_issued - 1 - j) / 3 + 1 : 0;   // fills of buffer j
+        if (nf) mbar_drain(bar(B_FULLQ + j), (nf - 1) & 1);
       }
     }
     if (warp == 8 && lane == 0) {
@@ -707,13 +870,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 template <int D>
-cudaError_t launch_d(dim3 grid, size_t tail, const LayerInfo &L, const TcParams &P, cudaStream_t s) {
-  const size_t smem = 1024 + Geo<D>::kOffRows + tail;
-  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+cudaError_t launch_d(dim3 grid, const LayerInfo &L, const CUtensorMap &tmq, const TcParams &P,
+                     cudaStream_t s) {
+  const size_t smem = 1024 + Geo<D>::kOffBars + B_COUNT * 8;
+  static_assert(1024 + Geo<128>::kOffBars + B_COUNT * 8 + sizeof(Item) * 2 + 16 <= 227 * 1024,
+                "shared memory of a CTA");
   cudaError_t e =
       cudaFuncSetAttribute(k_extend_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_extend_tc<D><<<grid, kThreads, smem, s>>>(L.tmk, L.tmv, P);
+  k_extend_tc<D><<<grid, kThreads, smem, s>>>(L.tmk, L.tmv, tmq, P);
   return cudaGetLastError();
 }
 
@@ -752,15 +917,17 @@ cudaError_t launch_attn_extend_tc(Ctx &c, const AttnArgs &a, cudaStream_t s) {
   P.sinks = a.sinks;
   P.scale_log2 = a.scale * 1.4426950408889634f;
   P.out = static_cast<__nv_bfloat16 *>(a.out);
-  P.max_pages = a.max_seq_len / P.ps + kKeys / P.ps + 2;
   P.err = c.err_word;
   // Persistent: one CTA per SM (the KV heads share the SMs), each looping
   // over its items.
   const int per_head = std::max(1, (c.num_sms > 0 ? c.num_sms : 148) / L.hkv);
   dim3 grid(std::min(P.items_upper, per_head), L.hkv);
-  const size_t tail = ((size_t)P.max_pages * 4 + 7) / 8 * 8 + B_COUNT * 8;
-  if (c.cfg.head_dim == 64) return launch_d<64>(grid, tail, L, P, s);
-  return launch_d<128>(grid, tail, L, P, s);
+  // Q as a [nq][Hq][D] tensor, one box = one Q tile of a KV head's G heads.
+  CUtensorMap tmq;
+  if (!make_q_tensor_map(&tmq, a.q, a.nq, c.cfg.num_q_heads, c.cfg.head_dim, P.G))
+    return cudaErrorInvalidValue;
+  if (c.cfg.head_dim == 64) return launch_d<64>(grid, L, tmq, P, s);
+  return launch_d<128>(grid, L, tmq, P, s);
 }
 
 }  // namespace swa
