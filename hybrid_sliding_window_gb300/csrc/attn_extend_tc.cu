@@ -644,6 +644,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + grp * 128 + lane_off;
     const uint32_t tO = tmem + 256 + grp * kD + lane_off;
     const int Hq = P.hkv * G;
+    // The row's sink logit in log2 units (its head is fixed for the CTA's life).
+    const float sg2 = P.sinks ? P.sinks[kvh * G + g] * 1.4426950408889634f : -INFINITY;
     int tg = 0, nd = 0;
     for (;;) {
       const int slot = nd & 1;
@@ -783,8 +785,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- epilogue ----
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_ODONE + grp), nd & 1, &s_abort))) break;
       tc_fence_after();
-      float sg2 = -INFINITY;
-      if (P.sinks) sg2 = P.sinks[kvh * G + g] * 1.4426950408889634f;
       const float mr = m_run == -INFINITY ? 0.f : m_run;
       const float mfin = fmaxf(mr, sg2);
       const float rsc = exp2f(mr - mfin);
