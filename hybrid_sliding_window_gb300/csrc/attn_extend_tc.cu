@@ -169,6 +169,23 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, 
                : "memory");
 }
 
+// Bulk tensor store of a box from shared memory (tracked by the issuing
+// thread's bulk async-group), its commit, and the waits for the group's
+// shared-memory reads (the source may be reused) or for its completion.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int c0, int c1, int c2,
+                                             uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];\n" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+
 // tcgen05 shared-memory matrix descriptor: start >> 4 at [0,14), leading byte
 // offset >> 4 at [16,30), stride byte offset >> 4 at [32,46), version 1 at
 // [46,48), layout 2 (128-byte swizzle) at [61,64).
@@ -266,12 +283,20 @@ __device__ __forceinline__ int64_t key_lo(int kind, int window, int64_t p) {
   return (p / window) * window;
 }
 
+// (row r, 16-byte chunk c) of a 128-row tile of D bf16 columns stored as D / 64
+// blocks of [128 rows][128 B] with the 128-byte swizzle: the layout in which
+// TMA writes a Q tile and reads an output tile.
+__device__ __forceinline__ uint32_t tile_off(int r, int c) {
+  return (uint32_t)((c >> 3) * kBlock + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
 // Shared memory (offsets from a 1024-byte aligned base): Geo<D>, then the
 // mbarriers.  FULLQ / QFREE belong to the three Q buffers, IFULL / IEMPTY to
-// the two-slot ring through which the producer hands items to the others.
+// the two-slot ring through which the producer hands items to the others,
+// STAGED to each softmax group's output tile staged for its bulk store.
 enum { B_FULLK = 0, B_EMPTYK = 2, B_FULLV = 4, B_EMPTYV = 6, B_SDONE = 8, B_PREADY = 10,
-       B_ODONE = 12, B_FULLQ = 14, B_QFREE = 17, B_IFULL = 20, B_IEMPTY = 22, B_DRAIN = 24,
-       B_COUNT = 25 };
+       B_ODONE = 12, B_FULLQ = 14, B_QFREE = 17, B_IFULL = 20, B_IEMPTY = 22, B_STAGED = 24,
+       B_DRAIN = 26, B_COUNT = 27 };
 constexpr int kItemReaders = 9;              // the 8 softmax warps and the MMA lane
 
 // A work item: 2T consecutive query tokens of request b (clipped to the end
@@ -356,10 +381,16 @@ __device__ __forceinline__ int32_t page_first_row(bool full, int ps_shift, int64
   return (int32_t)(page * page_stride);
 }
 
-template <int kD>
+// kWin: a sliding-window or chunked layer, whose key tiles mostly straddle a
+// window or causal edge; its softmax decides the masks per 64-key chunk and
+// skips chunks outside every row's range.  Full layers (kWin false) mask per
+// key tile, which keeps their loop - the one that sets the pace of the long
+// causal rows - smaller in the instruction cache.
+template <int kD, bool kWin>
 __global__ void __launch_bounds__(kThreads, 1)
     k_extend_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                const __grid_constant__ CUtensorMap tmQ, TcParams P) {
+                const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
+                TcParams P) {
   using Gm = Geo<kD>;
   constexpr int kTileBytes = Gm::kTileBytes, kOffQ = Gm::kOffQ, kOffK = Gm::kOffK;
   constexpr int kOffV = Gm::kOffV, kCPR = Gm::kCPR;
@@ -398,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_ODONE + i), 1);
       mbar_init(bar(B_IFULL + i), 1);
       mbar_init(bar(B_IEMPTY + i), kItemReaders);
+      mbar_init(bar(B_STAGED + i), kRows);
     }
     for (int j = 0; j < 3; ++j) {
       mbar_init(bar(B_FULLQ + j), 1);
@@ -646,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int Hq = P.hkv * G;
     // The row's sink logit in log2 units (its head is fixed for the CTA's life).
     const float sg2 = P.sinks ? P.sinks[kvh * G + g] * 1.4426950408889634f : -INFINITY;
-    int tg = 0, nd = 0;
+    int tg = 0, nd = 0, n_staged = 0;
     for (;;) {
       const int slot = nd & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_IFULL + slot), (nd >> 1) & 1, &s_abort)))
@@ -674,11 +706,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int e_hi = edge ? (row_valid ? (int)max((int64_t)-1, min((int64_t)kKeys - 1, p_row - j0))
                                            : -1)
                               : kKeys - 1;
-        // Interior tiles (no row of the warp at a window or causal edge) skip
-        // the per-key masks entirely.
-        const bool masked = __any_sync(0xffffffffu, edge);
-        // Keys outside this row's range read as -inf (edge tiles only): the
-        // max and the exponentials below then need no per-key test.
+        // Keys outside this row's range read as -inf where some row of the warp
+        // has a window or causal edge (per tile on full layers, per 64-key
+        // chunk on windowed ones): the max and the exponentials below then
+        // need no per-key test.
+        const bool masked = !kWin && __any_sync(0xffffffffu, edge);
         auto mask_in_place = [&](uint32_t (&rr)[64], int cb) {
   #pragma unroll
           for (int e = 0; e < 64; ++e) {
@@ -699,11 +731,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t acc2[2] = {0ull, 0ull};   // running pair sums (two chains)
   #pragma unroll 1
         for (int cb = 0; cb < 2; ++cb) {
+          const int c0 = cb * 64;
+          // On windowed layers a chunk outside every row's range (a window's
+          // far side, the causal future) has all-zero weights: P = 0 and
+          // nothing accumulates.
+          if (kWin && __all_sync(0xffffffffu, e_hi < c0 || e_lo > c0 + 63)) {
+            uint32_t zero[32];
+  #pragma unroll
+            for (int e = 0; e < 32; ++e) zero[e] = 0u;
+            TC_ST32(tS + cb * 32, zero);
+            continue;
+          }
           uint32_t rr[64];
           TC_LD32(tS + cb * 64, rr);        // two loads in flight before one wait
           TC_LD32(tS + cb * 64 + 32, (rr + 32));
           tc_wait_ld();
-          if (masked) mask_in_place(rr, cb);
+          if (kWin ? __any_sync(0xffffffffu, e_lo > c0 || e_hi < c0 + 63) : masked)
+            mask_in_place(rr, cb);
           // four independent chains of three-input maxima
           float m2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
   #pragma unroll
@@ -790,11 +834,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float rsc = exp2f(mr - mfin);
       const float denom = l_run * rsc + (P.sinks ? exp2f(sg2 - mfin) : 0.f);
       const float f = denom > 0.f ? rsc / denom : 0.f;
-      // The warp's 32 output rows go through shared memory (this tile's Q
-      // buffer: every product that read it has completed by ODONE), so that
-      // the global stores are whole rows written by consecutive lanes.
+      // The output rows go through shared memory (this tile's Q buffer:
+      // every product that read it has completed by ODONE).  On windowed
+      // layers, whose items are short, a tile whose rows are all tokens of
+      // the item is staged in the TMA layout and written by one bulk tensor
+      // store; otherwise (full layers; a ragged tile at the end of a
+      // request's chunk) the warps store the valid rows.
       const int jq = (2 * nd + grp) % 3;
-      char *stage = smem + kOffQ + jq * kTileBytes + (warp & 3) * 32 * (kD * 2);
+      char *qbuf = smem + kOffQ + jq * kTileBytes;
+      const bool whole = kWin && grp * T + T <= it.n_tok;
+      char *stage = qbuf + (warp & 3) * 32 * (kD * 2);
 #pragma unroll 1
       for (int cb = 0; cb < kD / 64; ++cb) {
         uint32_t rr[64];
@@ -811,31 +860,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             w[k] = *reinterpret_cast<uint32_t *>(&h);
           }
           const int c = (cb * 64 + e) >> 3;   // 16-byte chunk of the row
-          *reinterpret_cast<uint4 *>(stage + lane * (kD * 2) + ((c ^ (lane & (kCPR - 1))) << 4)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
+          char *dst = whole ? qbuf + tile_off(r, c)
+                            : stage + lane * (kD * 2) + ((c ^ (lane & (kCPR - 1))) << 4);
+          *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      __syncwarp();
+      if (whole) {
+        // Generic-proxy writes made visible to the bulk copy, then handed to
+        // the group's first thread, which issues the store and releases the
+        // buffer once the copy has read it.
+        fence_async_smem();
+        mbar_arrive(bar(B_STAGED + grp));
+        if ((tid & 127) == 0) {
+          if (mbar_wait(bar(B_STAGED + grp), n_staged & 1, &s_abort)) {
+            for (int h = 0; h < kD / 64; ++h)
+              tma_store_3d(&tmO, h * 64, kvh * G, (int)(it.q0 + grp * T),
+                           sb + kOffQ + jq * kTileBytes + h * kBlock);
+            bulk_commit();
+            bulk_wait_read();
+          }
+        }
+        ++n_staged;
+      } else {
+        __syncwarp();
 #pragma unroll 4
-      for (int idx = lane; idx < 32 * kCPR; idx += 32) {
-        const int i = idx / kCPR, c = idx % kCPR;
-        const int rw = (warp & 3) * 32 + i;     // row of Q tile grp
-        const int trw = grp * T + rw / G;
-        if (trw < it.n_tok) {
-          const uint4 v =
-              *reinterpret_cast<const uint4 *>(stage + i * (kD * 2) + ((c ^ (i & (kCPR - 1))) << 4));
-          *reinterpret_cast<uint4 *>(P.out + ((it.q0 + trw) * Hq + kvh * G + rw % G) * kD + c * 8) =
-              v;
+        for (int idx = lane; idx < 32 * kCPR; idx += 32) {
+          const int i = idx / kCPR, c = idx % kCPR;
+          const int rw = (warp & 3) * 32 + i;     // row of Q tile grp
+          const int trw = grp * T + rw / G;
+          if (trw < it.n_tok) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(stage + i * (kD * 2) +
+                                                             ((c ^ (i & (kCPR - 1))) << 4));
+            *reinterpret_cast<uint4 *>(P.out + ((it.q0 + trw) * Hq + kvh * G + rw % G) * kD +
+                                       c * 8) = v;
+          }
         }
+        // The buffer's next contents arrive by TMA (the async proxy): order
+        // these accesses before it.
+        fence_async_smem();
       }
-      // The buffer's next contents arrive by TMA (the async proxy): order
-      // these accesses before it, then release the buffer.
-      fence_async_smem();
       mbar_arrive(bar(B_QFREE + jq));
       tg += it.n_tiles;
       ++nd;
     }
   }
+  // The output stores complete before the CTA exits.
+  if (kWin && warp < 8 && (tid & 127) == 0) bulk_wait_all();
   // Every role has left its loop: s_abort is final.
   __syncthreads();
   if (s_abort) {
@@ -869,16 +939,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int D>
-cudaError_t launch_d(dim3 grid, const LayerInfo &L, const CUtensorMap &tmq, const TcParams &P,
-                     cudaStream_t s) {
+template <int D, bool kWin>
+cudaError_t launch_d(dim3 grid, const LayerInfo &L, const CUtensorMap &tmq, const CUtensorMap &tmo,
+                     const TcParams &P, cudaStream_t s) {
   const size_t smem = 1024 + Geo<D>::kOffBars + B_COUNT * 8;
-  static_assert(1024 + Geo<128>::kOffBars + B_COUNT * 8 + sizeof(Item) * 2 + 16 <= 227 * 1024,
+  static_assert(1024 + Geo<128>::kOffBars + B_COUNT * 8 + sizeof(Item) * 2 + 2 * 32 * 4 + 16 <=
+                    227 * 1024,
                 "shared memory of a CTA");
   cudaError_t e =
-      cudaFuncSetAttribute(k_extend_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      cudaFuncSetAttribute(k_extend_tc<D, kWin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_extend_tc<D><<<grid, kThreads, smem, s>>>(L.tmk, L.tmv, tmq, P);
+  k_extend_tc<D, kWin><<<grid, kThreads, smem, s>>>(L.tmk, L.tmv, tmq, tmo, P);
   return cudaGetLastError();
 }
 
@@ -922,12 +993,17 @@ cudaError_t launch_attn_extend_tc(Ctx &c, const AttnArgs &a, cudaStream_t s) {
   // over its items.
   const int per_head = std::max(1, (c.num_sms > 0 ? c.num_sms : 148) / L.hkv);
   dim3 grid(std::min(P.items_upper, per_head), L.hkv);
-  // Q as a [nq][Hq][D] tensor, one box = one Q tile of a KV head's G heads.
-  CUtensorMap tmq;
-  if (!make_q_tensor_map(&tmq, a.q, a.nq, c.cfg.num_q_heads, c.cfg.head_dim, P.G))
+  // Q and the output as [nq][Hq][D] tensors, one box = one 128-row tile of a
+  // KV head's G heads.
+  CUtensorMap tmq, tmo;
+  if (!make_qo_tensor_map(&tmq, a.q, a.nq, c.cfg.num_q_heads, c.cfg.head_dim, P.G) ||
+      !make_qo_tensor_map(&tmo, a.out, a.nq, c.cfg.num_q_heads, c.cfg.head_dim, P.G))
     return cudaErrorInvalidValue;
-  if (c.cfg.head_dim == 64) return launch_d<64>(grid, L, tmq, P, s);
-  return launch_d<128>(grid, L, tmq, P, s);
+  const bool win = L.kind != SWA_LAYER_FULL;
+  if (c.cfg.head_dim == 64)
+    return win ? launch_d<64, true>(grid, L, tmq, tmo, P, s) : launch_d<64, false>(grid, L, tmq, tmo, P, s);
+  return win ? launch_d<128, true>(grid, L, tmq, tmo, P, s)
+             : launch_d<128, false>(grid, L, tmq, tmo, P, s);
 }
 
 }  // namespace swa

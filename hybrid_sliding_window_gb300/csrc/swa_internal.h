@@ -203,10 +203,10 @@ bool tc_extend_supported(const Ctx &c, int layer);
 // 128- or 256-byte head rows, page size 16..128); leaves tma = false when the
 // layer does not qualify or encoding fails.
 void make_kv_tensor_maps(Ctx &c, int layer);
-// TMA tensor map over the queries q [nq][hq][d] (bf16) whose box is one
-// 128-row Q tile: {64 dims, g heads, 128 / g tokens}, 128-byte swizzle.
-// False if q is not 16-byte aligned or encoding fails.
-bool make_q_tensor_map(CUtensorMap *m, const void *q, int64_t nq, int hq, int d, int g);
+// TMA tensor map over an extend call's queries or outputs, x [nq][hq][d]
+// (bf16), whose box is one 128-row tile: {64 dims, g heads, 128 / g tokens},
+// 128-byte swizzle.  False if x is not 16-byte aligned or encoding fails.
+bool make_qo_tensor_map(CUtensorMap *m, const void *x, int64_t nq, int hq, int d, int g);
 size_t tc_extend_ws_bytes(const Ctx &c, int layer, int64_t n_tokens, int max_seq_len);
 cudaError_t launch_attn_extend_tc(Ctx &c, const AttnArgs &a, cudaStream_t s);
 

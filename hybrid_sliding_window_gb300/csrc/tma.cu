@@ -1,5 +1,5 @@
 // TMA tensor maps over one layer's K and V rows, built once per context, and
-// over an extend call's queries, built per call.
+// over an extend call's queries and outputs, built per call.
 //
 // A layer's K (or V) rows form a dense [rows][Hkv][D] array: the per-layer
 // pool, or the layer's view of the page-major envelope (row = kernel-facing
@@ -65,14 +65,14 @@ void make_kv_tensor_maps(Ctx &c, int layer) {
   L.tma = true;
 }
 
-bool make_q_tensor_map(CUtensorMap *m, const void *q, int64_t nq, int hq, int d, int g) {
+bool make_qo_tensor_map(CUtensorMap *m, const void *x, int64_t nq, int hq, int d, int g) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-  if (!fn || nq <= 0 || ((uintptr_t)q & 15) || g <= 0 || 128 % g) return false;
+  if (!fn || nq <= 0 || ((uintptr_t)x & 15) || g <= 0 || 128 % g) return false;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hq, (cuuint64_t)nq};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)hq * d * 2};
   cuuint32_t box[3] = {64, (cuuint32_t)g, (cuuint32_t)(128 / g)};
   cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, estr,
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(x), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
