@@ -75,3 +75,23 @@ def test_extend_gptoss_shaped_head_dim_64(ps, path, expect):
     for l, (g, o) in res.items():
         assert_close(g, o, 2e-2, f"D=64 ps={ps} layer {l}")
     assert api.swa_device_check(P.ctx) == 0
+
+
+CHUNKED_LAYERS = [(OT.CHUNKED, 192, 8), (OT.SLIDING, 63, 8), (OT.FULL, 0, 4)]
+
+
+@pytest.mark.parametrize("ps", [16, 64])
+@pytest.mark.parametrize("path,expect", [pytest.param(-1, 2, id="tcgen05"),
+                                         pytest.param(0, 0, id="generic")])
+def test_extend_chunked_local_and_short_window(ps, path, expect):
+    """Chunked-local attention (keys from the start of the query's 192-token
+    chunk: chunk starts fall inside work items and inside 128-key tiles) and a
+    64-key sliding window, next to a full layer: the tensor-core kernel's
+    windowed instance (per-64-key-chunk masks, chunks outside every row's
+    range skipped, whole output tiles by bulk store, ragged ones by the
+    warps)."""
+    P, res = _run(ps, path, prompt=[700, 333, 0], chunk=[150, 77, 40], layers=CHUNKED_LAYERS)
+    assert api.swa_last_attn_path(P.ctx) == expect
+    for l, (g, o) in res.items():
+        assert_close(g, o, 2e-2, f"chunked ps={ps} layer {l}")
+    assert api.swa_device_check(P.ctx) == 0
