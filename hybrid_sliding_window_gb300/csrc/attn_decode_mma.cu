@@ -361,6 +361,11 @@ __global__ void __launch_bounds__(NW * 32, (Smem<D, FP8, KM, NW>::kMinBlocks))
 
   // The previous kernel's memory is needed from here on.
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  // The next kernel on the stream may launch once every CTA of this grid has
+  // got here (all of them are resident by then): its CTAs read their own
+  // index tables while this grid streams, and wait for it to complete before
+  // touching anything it writes.
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
   // ---- Q rows into registers: their latency hides behind the first tile
   // loads ----
@@ -720,9 +725,6 @@ __global__ void __launch_bounds__(NW * 32, (Smem<D, FP8, KM, NW>::kMinBlocks))
     }
   }
   cp_wait<0>();
-  // This CTA's reads are done: the next kernel on the stream may start its
-  // launch (its CTAs wait for this grid to finish before touching memory).
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   if constexpr (KM) {
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {

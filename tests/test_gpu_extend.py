@@ -95,3 +95,36 @@ def test_extend_chunked_local_and_short_window(ps, path, expect):
     for l, (g, o) in res.items():
         assert_close(g, o, 2e-2, f"chunked ps={ps} layer {l}")
     assert api.swa_device_check(P.ctx) == 0
+
+
+def test_extend_many_requests():
+    """40 requests in one call - the producer's request scan spans two
+    32-request batches - with prefixes of 0 to 299 tokens and chunks of 0 to 69
+    (three empty ones): the tensor-core kernel against the oracle."""
+    rng = np.random.default_rng(5)
+    n = 40
+    P = Pair(LAYERS, Hq=64, D=128, dtype="bf16", ps=16, size_full=16 * (n * 400 // 16 + 40),
+             size_swa=16 * (n * 320 // 16 + 40), seed=13, perm_free=True, max_ctx=512,
+             max_reqs=n + 1)
+    rows = list(range(1, n + 1))
+    prompt = rng.integers(0, 300, n).astype(np.int64)
+    chunk = rng.integers(0, 70, n).astype(np.int64)
+    chunk[[3, 17, 33]] = 0
+    lens = np.zeros(n, np.int64)
+    ev = np.zeros(n, np.int64)
+    while (lens < prompt).any():
+        sel = [i for i in range(n) if lens[i] < prompt[i]]
+        e = ev[sel].copy()
+        P.evict([rows[i] for i in sel], lens[sel], e, 0)
+        ev[sel] = e
+        new = np.minimum(lens[sel] + 128, prompt[sel])
+        P.extend([rows[i] for i in sel], lens[sel], new)
+        lens[sel] = new
+    P.evict(rows, lens, ev, 0)
+    seq = lens + chunk
+    P.extend(rows, lens, seq)
+    res = P.extend_attention(rows, lens, seq)
+    assert api.swa_last_attn_path(P.ctx) == 2
+    for l, (g, o) in res.items():
+        assert_close(g, o, 2e-2, f"40 requests layer {l}")
+    assert api.swa_device_check(P.ctx) == 0
