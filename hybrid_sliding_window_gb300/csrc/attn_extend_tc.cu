@@ -1,6 +1,6 @@
 // Chunked-prefill (extend) attention on the 5th-generation tensor cores
 // (tcgen05 + TMEM + TMA), bf16 KV in the per-layer layout, D = 64 or 128,
-// GQA group G in {8, 16}, page size 16..64 (a power of two).
+// any GQA group G up to 128, page size 16..64 (a power of two).
 //
 // Method: "SWA in SGLang" design note - the chunk's queries at positions
 // pre..seq-1 attend causally; sliding layers see the last Wx+1 keys, full
@@ -10,14 +10,15 @@
 // warp-specialised; TMEM and barriers set up once per CTA, barrier phases
 // following running counts, so that no role waits for the others at an item
 // boundary):
-//   * an item is two 128-row Q tiles, each (128/G) consecutive query tokens
-//     x the G query heads of one KV head, so every K/V tile it loads feeds two
-//     QK^T and two PV products;
+//   * an item is two Q tiles of up to 128 rows, each floor(128/G) consecutive
+//     query tokens x the G query heads of one KV head (the tile's last 128 mod
+//     G rows, if any, are unused rows whose weights are zero), so every K/V
+//     tile it loads feeds two QK^T and two PV products;
 //   * warp 9 finds each item (a warp-wide prefix count over the requests),
 //     derives its key tiles and hands it to the other roles through a
 //     two-slot ring in shared memory (so that their loops carry no per-item
 //     arithmetic); it loads the Q tiles with TMA (box {64 dims, G heads,
-//     128/G tokens}) into three rotating buffers - a buffer is released by
+//     floor(128/G) tokens}) into three rotating buffers - a buffer is released by
 //     the epilogue that staged its tile's output through it, so the next
 //     item's first tile is loaded while the current item still computes -
 //     looks up page rows 32 page slots at a time with its lanes, a batch
@@ -407,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kvh = blockIdx.y;
   const int G = P.G;
   const int T = kRows / G;                 // tokens per Q tile
+  const int TG = T * G;                    // rows of a Q tile in use (128 unless G divides it not)
   const int T2 = 2 * T;                    // tokens per item
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
@@ -480,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j = u % 3, f = u / 3;
       if (f >= 1 && !wait_all(bar(B_QFREE + j), (f - 1) & 1)) return false;
       if (lane == 0) {
-        mbar_expect_tx(bar(B_FULLQ + j), (uint32_t)kTileBytes);
+        mbar_expect_tx(bar(B_FULLQ + j), (uint32_t)(TG * 128 * (kD / 64)));
         for (int h = 0; h < kD / 64; ++h)
           tma_load_3d(sb + kOffQ + j * kTileBytes + h * kBlock, &tmQ, h * 64, kvh * G, (int)tok,
                       bar(B_FULLQ + j));
@@ -687,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_IEMPTY + slot));
       if (it.b < 0) break;
-      const bool row_valid = tr < it.n_tok;
+      const bool row_valid = r < TG && tr < it.n_tok;
       const int64_t p_row = it.pfirst + tr;
       const int64_t lo_row = key_lo(P.kind, P.window, p_row);
       float m_run = -INFINITY, l_run = 0.f;
@@ -888,7 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int i = idx / kCPR, c = idx % kCPR;
           const int rw = (warp & 3) * 32 + i;     // row of Q tile grp
           const int trw = grp * T + rw / G;
-          if (trw < it.n_tok) {
+          if (rw < TG && trw < it.n_tok) {
             const uint4 v = *reinterpret_cast<const uint4 *>(stage + i * (kD * 2) +
                                                              ((c ^ (i & (kCPR - 1))) << 4));
             *reinterpret_cast<uint4 *>(P.out + ((it.q0 + trw) * Hq + kvh * G + rw % G) * kD +
@@ -958,7 +960,7 @@ bool tc_extend_supported(const Ctx &c, int layer) {
       (c.cfg.head_dim != 64 && c.cfg.head_dim != 128) || c.cfg.page_size > 64)
     return false;
   const int G = c.cfg.num_q_heads / c.layers[layer].hkv;
-  return G == 8 || G == 16;
+  return G >= 1 && G <= kRows;
 }
 
 size_t tc_extend_ws_bytes(const Ctx &, int, int64_t, int) { return 256; }

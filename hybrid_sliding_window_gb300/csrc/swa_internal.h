@@ -204,8 +204,9 @@ bool tc_extend_supported(const Ctx &c, int layer);
 // layer does not qualify or encoding fails.
 void make_kv_tensor_maps(Ctx &c, int layer);
 // TMA tensor map over an extend call's queries or outputs, x [nq][hq][d]
-// (bf16), whose box is one 128-row tile: {64 dims, g heads, 128 / g tokens},
-// 128-byte swizzle.  False if x is not 16-byte aligned or encoding fails.
+// (bf16), whose box is one tile of up to 128 rows: {64 dims, g heads,
+// 128 / g tokens}, 128-byte swizzle.  False if x is not 16-byte aligned, g is
+// outside 1..128 or encoding fails.
 bool make_qo_tensor_map(CUtensorMap *m, const void *x, int64_t nq, int hq, int d, int g);
 size_t tc_extend_ws_bytes(const Ctx &c, int layer, int64_t n_tokens, int max_seq_len);
 cudaError_t launch_attn_extend_tc(Ctx &c, const AttnArgs &a, cudaStream_t s);

@@ -67,7 +67,7 @@ void make_kv_tensor_maps(Ctx &c, int layer) {
 
 bool make_qo_tensor_map(CUtensorMap *m, const void *x, int64_t nq, int hq, int d, int g) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-  if (!fn || nq <= 0 || ((uintptr_t)x & 15) || g <= 0 || 128 % g) return false;
+  if (!fn || nq <= 0 || ((uintptr_t)x & 15) || g <= 0 || g > 128) return false;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hq, (cuuint64_t)nq};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)hq * d * 2};
   cuuint32_t box[3] = {64, (cuuint32_t)g, (cuuint32_t)(128 / g)};

@@ -19,8 +19,8 @@ LAYERS = [(OT.SLIDING, 127, 8), (OT.FULL, 0, 4)]
 GPTOSS_LAYERS = [(OT.SLIDING, 127, 8), (OT.FULL, 0, 8)]      # G = 8, D = 64
 
 
-def _run(ps, path, prompt, chunk, layers=LAYERS, chunk0=256, D=128):
-    P = Pair(layers, Hq=64, D=D, dtype="bf16", ps=ps, size_full=ps * (4096 // ps + 40),
+def _run(ps, path, prompt, chunk, layers=LAYERS, chunk0=256, D=128, Hq=64):
+    P = Pair(layers, Hq=Hq, D=D, dtype="bf16", ps=ps, size_full=ps * (4096 // ps + 40),
              size_swa=ps * (1536 // ps + 40), seed=11, perm_free=True, max_ctx=4096, max_reqs=4)
     api.swa_set_attn_path(P.ctx, path)
     rows = [1, 2, 3]
@@ -127,4 +127,21 @@ def test_extend_many_requests():
     assert api.swa_last_attn_path(P.ctx) == 2
     for l, (g, o) in res.items():
         assert_close(g, o, 2e-2, f"40 requests layer {l}")
+    assert api.swa_device_check(P.ctx) == 0
+
+
+@pytest.mark.parametrize("Hq,layers", [
+    pytest.param(40, [(OT.SLIDING, 127, 8), (OT.CHUNKED, 192, 8), (OT.FULL, 0, 8)], id="G5"),
+    pytest.param(24, [(OT.SLIDING, 63, 8), (OT.FULL, 0, 8)], id="G3"),
+    pytest.param(8, [(OT.SLIDING, 63, 8), (OT.FULL, 0, 8)], id="G1"),
+])
+def test_extend_group_sizes_not_dividing_128(Hq, layers):
+    """GQA groups whose Q tiles leave rows unused (G = 5: 25 tokens x 5 heads =
+    125 rows, G = 3: 126) or hold 128 tokens of one head (G = 1), on the
+    tensor-core kernel, against the oracle: Llama4-shaped heads (40 query, 8 KV)
+    with bf16 KV, sliding, chunked-local and full layers."""
+    P, res = _run(64, -1, prompt=[700, 333, 0], chunk=[150, 77, 40], layers=layers, Hq=Hq)
+    assert api.swa_last_attn_path(P.ctx) == 2
+    for l, (g, o) in res.items():
+        assert_close(g, o, 2e-2, f"Hq={Hq} layer {l}")
     assert api.swa_device_check(P.ctx) == 0
