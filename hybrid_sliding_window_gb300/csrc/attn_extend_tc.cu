@@ -49,6 +49,7 @@
 #include <algorithm>
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -60,6 +61,7 @@ namespace {
 constexpr int kRows = 128;                   // rows of one Q tile (M)
 constexpr int kKeys = 128;                   // keys per K/V tile
 constexpr int kThreads = 320;                // 8 softmax warps + MMA warp + load warp
+constexpr int kThreadsF8 = 384;              // ... + 2 warps converting E4M3 K/V and Q to f16
 constexpr int kBlock = kRows * 64 * 2;       // one 64-column block of a 128-row tile (16 KB)
 // A 128-row (or 128-key) tile of D bf16 columns: D / 64 blocks of
 // [128 rows][128 B] with the 128-byte swizzle.
@@ -93,6 +95,11 @@ struct TcParams {
   float scale_log2;
   __nv_bfloat16 *out;
   int32_t *err;
+  // E4M3 KV only: the layer's K and V rows (row r of head h at r * row_bytes +
+  // h * D bytes) and their dequantisation scales.
+  const uint8_t *k8, *v8;
+  int64_t row_bytes;
+  float k_scale, v_scale;
 };
 
 // ------------------------------------------------------------------ PTX ---
@@ -194,10 +201,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
   return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-// Instruction descriptor, kind::f16: D f32, A and B bf16, A K-major, B major
-// bit 16, N >> 3 at [17,23), M >> 4 at [24,29).
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+// Instruction descriptor, kind::f16: D f32, A and B bf16 (type 1 at [7,10) and
+// [10,13)) or both f16 (type 0), A K-major, B major bit 16, N >> 3 at [17,23),
+// M >> 4 at [24,29).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major, bool f16 = false) {
+  return (1u << 4) | (f16 ? 0u : (1u << 7) | (1u << 10)) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
@@ -284,6 +292,45 @@ __device__ __forceinline__ int64_t key_lo(int kind, int window, int64_t p) {
   return (p / window) * window;
 }
 
+// E4M3 KV: four E4M3 values (bytes 0..3 of w) to two f16 pairs, low byte in
+// the low half (exact: E4M3 is a subset of f16); a bf16 pair to an f16 pair
+// (queries; round to nearest); a 16-byte read-only global load.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
+  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x));
+  __half2 h = __floats2half2_rn(f.x, f.y);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint4 ld_nc16(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+// P = exp2(...) packed as the MMA's A type: bf16 pairs, or f16 pairs (E4M3 KV,
+// whose operands are f16), and back.
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack_p(float a, float b) {
+  if constexpr (kF16) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+  }
+}
+template <bool kF16>
+__device__ __forceinline__ float2 unpack_p(uint32_t x) {
+  if constexpr (kF16) return __half22float2(*reinterpret_cast<const __half2 *>(&x));
+  else return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x));
+}
+
 // (row r, 16-byte chunk c) of a 128-row tile of D bf16 columns stored as D / 64
 // blocks of [128 rows][128 B] with the 128-byte swizzle: the layout in which
 // TMA writes a Q tile and reads an output tile.
@@ -294,11 +341,12 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
 // Shared memory (offsets from a 1024-byte aligned base): Geo<D>, then the
 // mbarriers.  FULLQ / QFREE belong to the three Q buffers, IFULL / IEMPTY to
 // the two-slot ring through which the producer hands items to the others,
-// STAGED to each softmax group's output tile staged for its bulk store.
+// STAGED to each softmax group's output tile staged for its bulk store, QCONV
+// (E4M3 KV) to the Q buffers converted to f16 in place.
 enum { B_FULLK = 0, B_EMPTYK = 2, B_FULLV = 4, B_EMPTYV = 6, B_SDONE = 8, B_PREADY = 10,
        B_ODONE = 12, B_FULLQ = 14, B_QFREE = 17, B_IFULL = 20, B_IEMPTY = 22, B_STAGED = 24,
-       B_DRAIN = 26, B_COUNT = 27 };
-constexpr int kItemReaders = 9;              // the 8 softmax warps and the MMA lane
+       B_DRAIN = 26, B_QCONV = 27, B_COUNT = 30 };
+constexpr int kItemReaders = 9;              // the 8 softmax warps and the MMA lane (+2 converters)
 
 // A work item: 2T consecutive query tokens of request b (clipped to the end
 // of its chunk, qend), starting at token q0 and key position pfirst, with its
@@ -387,12 +435,19 @@ __device__ __forceinline__ int32_t page_first_row(bool full, int ps_shift, int64
 // skips chunks outside every row's range.  Full layers (kWin false) mask per
 // key tile, which keeps their loop - the one that sets the pace of the long
 // causal rows - smaller in the instruction cache.
-template <int kD, bool kWin>
-__global__ void __launch_bounds__(kThreads, 1)
+//
+// kF8: E4M3 KV.  Two more warps (10, 11) read the K/V rows with plain loads
+// (through their own page lookups), convert them to f16 (exact) into the
+// stage buffers, and convert each Q tile to f16 in place once TMA has landed
+// it; the MMAs then run with f16 operands, P is packed as f16, the K scale
+// joins the softmax scale and the V scale the output normalisation.
+template <int kD, bool kWin, bool kF8>
+__global__ void __launch_bounds__(kF8 ? kThreadsF8 : kThreads, 1)
     k_extend_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
                 TcParams P) {
   using Gm = Geo<kD>;
+  static_assert(!kF8 || kD == 128, "E4M3 KV: D = 128");
   constexpr int kTileBytes = Gm::kTileBytes, kOffQ = Gm::kOffQ, kOffK = Gm::kOffK;
   constexpr int kOffV = Gm::kOffV, kCPR = Gm::kCPR;
   extern __shared__ char smem_raw[];
@@ -422,20 +477,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(B_FULLK + i), 1);
+      mbar_init(bar(B_FULLK + i), kF8 ? 64 : 1);
       mbar_init(bar(B_EMPTYK + i), 1);
-      mbar_init(bar(B_FULLV + i), 1);
+      mbar_init(bar(B_FULLV + i), kF8 ? 64 : 1);
       mbar_init(bar(B_EMPTYV + i), 1);
       mbar_init(bar(B_SDONE + i), 1);
       mbar_init(bar(B_PREADY + i), kRows);
       mbar_init(bar(B_ODONE + i), 1);
       mbar_init(bar(B_IFULL + i), 1);
-      mbar_init(bar(B_IEMPTY + i), kItemReaders);
+      mbar_init(bar(B_IEMPTY + i), kItemReaders + (kF8 ? 2 : 0));
       mbar_init(bar(B_STAGED + i), kRows);
     }
     for (int j = 0; j < 3; ++j) {
       mbar_init(bar(B_FULLQ + j), 1);
       mbar_init(bar(B_QFREE + j), kRows);
+      mbar_init(bar(B_QCONV + j), 64);
     }
     mbar_init(bar(B_DRAIN), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -443,8 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  constexpr uint32_t kIdS = idesc_f16(128, 128, false);
-  constexpr uint32_t kIdO = idesc_f16(128, kD, true);
+  constexpr uint32_t kIdS = idesc_f16(128, 128, false, kF8);
+  constexpr uint32_t kIdO = idesc_f16(128, kD, true, kF8);
 
   // Persistent: the producer takes items blockIdx.x, blockIdx.x + gridDim.x,
   // ... and publishes each one; the other roles follow the published order.
@@ -499,6 +555,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       it.n_tiles = g.n_tiles;
       it.kt0 = g.kt0;
       if (!(ok = publish(it))) break;
+      if constexpr (kF8) {
+        // E4M3 KV: the converter warps read K and V; only the Q tiles here.
+        const int u0 = 2 * (n_pub - 1);
+        if (!(ok = load_q(u0, it.q0))) break;
+        if (lane == 0 && it.q0 + T < it.qend)
+          for (int h = 0; h < kD / 64; ++h) tma_prefetch_3d(&tmQ, h * 64, kvh * G, (int)(it.q0 + T));
+        if (!(ok = load_q(u0 + 1, it.q0 + T))) break;
+        continue;
+      }
       const int64_t pg0 = g.kt0 >> P.ps_shift;
       const int n_pg = (int)((g.k_hi >> P.ps_shift) - pg0 + 1);
       const int n_slots = g.n_tiles * ppt;
@@ -632,10 +697,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t qa = dq0 + (uint64_t)((u0 % 3) * kTileBytes >> 4);
         const uint64_t qb = dq0 + (uint64_t)(((u0 + 1) % 3) * kTileBytes >> 4);
         if (!mbar_wait(bar(B_FULLK + (tg & 1)), (tg >> 1) & 1, &s_abort)) break;
-        if (!mbar_wait(bar(B_FULLQ + u0 % 3), (u0 / 3) & 1, &s_abort)) break;
+        if (!mbar_wait(bar((kF8 ? B_QCONV : B_FULLQ) + u0 % 3), (u0 / 3) & 1, &s_abort)) break;
         tc_fence_after();
         issue_s(0, qa, tg);
-        if (!mbar_wait(bar(B_FULLQ + (u0 + 1) % 3), ((u0 + 1) / 3) & 1, &s_abort)) break;
+        if (!mbar_wait(bar((kF8 ? B_QCONV : B_FULLQ) + (u0 + 1) % 3), ((u0 + 1) / 3) & 1,
+                       &s_abort))
+          break;
         tc_fence_after();
         issue_s(1, qb, tg);
         tc_commit(bar(B_EMPTYK + (tg & 1)));
@@ -668,6 +735,128 @@ __global__ void __launch_bounds__(kThreads, 1)
         tg += n_tiles;
         ++nd;
       }
+    }
+  } else if (warp >= 10) {
+    // ============ converters (E4M3 KV only): Q, K and V to f16 ============
+    // Per item: Q tile 0 (in place), then per key tile K and V into their
+    // stages, Q tile 1 after the first key tile.  Each K or V tile's 16-byte
+    // loads are issued before the wait for its stage, so their latency
+    // overlaps that wait (the converters run ahead of the tensor core).
+    const int ct = tid - kThreads;            // 0 .. 63
+    const int64_t max_page = P.pool_rows / P.ps - 1;
+    const int ppt = kKeys / P.ps;
+    auto wait_all = [&](uint32_t b, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(b, parity, &s_abort));
+    };
+    auto convert_q = [&](int u) {
+      const int j = u % 3;
+      if (!wait_all(bar(B_FULLQ + j), (u / 3) & 1)) return false;
+      char *buf = smem + kOffQ + j * kTileBytes;
+#pragma unroll 4
+      for (int i = ct; i < kTileBytes / 16; i += 64) {
+        uint4 *q16 = reinterpret_cast<uint4 *>(buf + i * 16);
+        uint4 v = *q16;
+        v.x = bf16x2_to_f16x2(v.x);
+        v.y = bf16x2_to_f16x2(v.y);
+        v.z = bf16x2_to_f16x2(v.z);
+        v.w = bf16x2_to_f16x2(v.w);
+        *q16 = v;
+      }
+      fence_async_smem();   // read by the tensor core (the async proxy)
+      mbar_arrive(bar(B_QCONV + j));
+      return true;
+    };
+    int tg = 0, nd = 0;
+    for (bool ok = true; ok;) {
+      const int slot = nd & 1;
+      if (!wait_all(bar(B_IFULL + slot), (nd >> 1) & 1)) break;
+      const Item it = s_item[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_IEMPTY + slot));
+      if (it.b < 0) break;
+      const int64_t k_lo = key_lo(P.kind, P.window, it.pfirst);
+      const int64_t k_hi = it.pfirst + it.n_tok - 1;
+      const int64_t pg0 = it.kt0 >> P.ps_shift;
+      const int n_pg = (int)((k_hi >> P.ps_shift) - pg0 + 1);
+      const int n_slots = it.n_tiles * ppt;
+      const bool full_layer = P.kind == SWA_LAYER_FULL;
+      const int32_t *rt_row = full_layer ? P.rt + P.req_idx[it.b] * P.rt_stride : nullptr;
+      const int32_t *pages = full_layer ? nullptr : P.plan.pages + (int64_t)it.b * P.plan.max_pages;
+      int64_t h0 = 0, h2 = 0, h3 = 0;
+      if (!full_layer) {
+        const int32_t *hdr = P.plan.hdr + it.b * 4;
+        h0 = hdr[0];
+        h2 = hdr[2];
+        h3 = hdr[3];
+      }
+      auto first_row = [&](int32_t rec) {
+        return page_first_row(full_layer, P.ps_shift, P.page_stride, max_page, rec, P.err);
+      };
+      // Slots outside the key range read the first in-range page (finite
+      // values, zero weight), as in the bf16 path.
+      const int32_t row_lo =
+          first_row(page_record(full_layer, P.ps_shift, rt_row, h0, h2, h3, pages, k_lo));
+      auto batch_rows = [&](int k) {   // lane i: row of page slot 32 k + i
+        const int i = 32 * k + lane;
+        const int64_t pos0 = (pg0 + i) << P.ps_shift;
+        const int64_t pos = pos0 > k_lo ? pos0 : k_lo;
+        return i < n_pg && pos <= k_hi && pos0 + P.ps > k_lo
+                   ? first_row(page_record(full_layer, P.ps_shift, rt_row, h0, h2, h3, pages, pos))
+                   : row_lo;
+      };
+      int32_t rows = batch_rows(0);
+      int cur_batch = 0;
+      // The 16 chunks of 16 E4M3 dims this thread converts of key tile t of
+      // K (kv = 0) or V: chunk idx = i * 64 + ct is key idx / 8, dims
+      // 16 (idx % 8) .. + 15.
+      auto load_tile = [&](int t, int kv, uint4 (&w)[16]) {
+        const int i0 = t * ppt;
+        if ((i0 >> 5) != cur_batch) {
+          cur_batch = i0 >> 5;
+          rows = batch_rows(cur_batch);
+        }
+        const uint8_t *src = (kv ? P.v8 : P.k8) + kvh * kD + (ct & 7) * 16;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int e = i * 8 + (ct >> 3);                 // key of the tile
+          const int32_t prow = __shfl_sync(0xffffffffu, rows, (i0 & 31) + (e >> P.ps_shift));
+          w[i] = ld_nc16(src + (int64_t)(prow + (e & (P.ps - 1))) * P.row_bytes);
+        }
+      };
+      auto store_tile = [&](int Tr, int kv, const uint4 (&w)[16]) {
+        const int st = Tr & 1;
+        if (Tr >= 2 && !wait_all(bar((kv ? B_EMPTYV : B_EMPTYK) + st), ((Tr >> 1) - 1) & 1))
+          return false;
+        char *dst = smem + (kv ? kOffV : kOffK) + st * kTileBytes;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int e = i * 8 + (ct >> 3), c = (ct & 7) * 2;   // f16 16-byte chunks c, c + 1
+          uint4 a, b;
+          e4m3x4_to_f16x4(w[i].x, a.x, a.y);
+          e4m3x4_to_f16x4(w[i].y, a.z, a.w);
+          e4m3x4_to_f16x4(w[i].z, b.x, b.y);
+          e4m3x4_to_f16x4(w[i].w, b.z, b.w);
+          *reinterpret_cast<uint4 *>(dst + tile_off(e, c)) = a;
+          *reinterpret_cast<uint4 *>(dst + tile_off(e, c + 1)) = b;
+        }
+        fence_async_smem();   // read by the tensor core (the async proxy)
+        mbar_arrive(bar((kv ? B_FULLV : B_FULLK) + st));
+        return true;
+      };
+      const int u0 = 2 * nd;
+      uint4 w[16];
+      load_tile(0, 0, w);
+      if (!(ok = convert_q(u0))) break;
+      for (int t = 0; t < it.n_tiles && ok; ++t) {
+        if (!(ok = store_tile(tg + t, 0, w))) break;
+        load_tile(t, 1, w);
+        if (!(ok = store_tile(tg + t, 1, w))) break;
+        if (t + 1 < it.n_tiles) load_tile(t + 1, 0, w);
+        if (t == 0) ok = convert_q(u0 + 1);
+      }
+      (void)n_slots;
+      tg += it.n_tiles;
+      ++nd;
     }
   } else {
     // ===================== softmax group i (warps 4i .. 4i+3) =====================
@@ -728,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // for the second chunk, the first chunk's P already in TMEM - before
         // this chunk's exponentials.  The 64-key loops stay rolled: one copy of
         // each body keeps the softmax code inside the instruction cache.
-        const float sc = P.scale_log2;
+        const float sc = kF8 ? P.scale_log2 * P.k_scale : P.scale_log2;
         const uint64_t sc2 = f2pack(sc, sc);
         uint64_t acc2[2] = {0ull, 0ull};   // running pair sums (two chains)
   #pragma unroll 1
@@ -785,10 +974,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_wait_ld();
   #pragma unroll
               for (int e = 0; e < 32; ++e) {
-                __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&pp[e]);
-                const float2 f = __bfloat1622float2(h);
-                h = __floats2bfloat162_rn(f.x * corr, f.y * corr);
-                pp[e] = *reinterpret_cast<uint32_t *>(&h);
+                const float2 f = unpack_p<kF8>(pp[e]);
+                pp[e] = pack_p<kF8>(f.x * corr, f.y * corr);
               }
               TC_ST32(tS, pp);
             }
@@ -812,8 +999,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float a0 = ex2(t0);
             const float a1 = ex2(t1);
             acc2[e & 1] = add2(acc2[e & 1], f2pack(a0, a1));
-            __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
-            pk[e] = *reinterpret_cast<uint32_t *>(&h);
+            pk[e] = pack_p<kF8>(a0, a1);
           }
           TC_ST32(tS + cb * 32, pk);
         }
@@ -835,7 +1021,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float mfin = fmaxf(mr, sg2);
       const float rsc = exp2f(mr - mfin);
       const float denom = l_run * rsc + (P.sinks ? exp2f(sg2 - mfin) : 0.f);
-      const float f = denom > 0.f ? rsc / denom : 0.f;
+      const float f = (denom > 0.f ? rsc / denom : 0.f) * (kF8 ? P.v_scale : 1.f);
       // The output rows go through shared memory (this tile's Q buffer:
       // every product that read it has completed by ODONE).  On windowed
       // layers, whose items are short, a tile whose rows are all tokens of
@@ -941,7 +1127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int D, bool kWin>
+template <int D, bool kWin, bool kF8>
 cudaError_t launch_d(dim3 grid, const LayerInfo &L, const CUtensorMap &tmq, const CUtensorMap &tmo,
                      const TcParams &P, cudaStream_t s) {
   const size_t smem = 1024 + Geo<D>::kOffBars + B_COUNT * 8;
@@ -949,15 +1135,18 @@ cudaError_t launch_d(dim3 grid, const LayerInfo &L, const CUtensorMap &tmq, cons
                     227 * 1024,
                 "shared memory of a CTA");
   cudaError_t e =
-      cudaFuncSetAttribute(k_extend_tc<D, kWin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      cudaFuncSetAttribute(k_extend_tc<D, kWin, kF8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
   if (e != cudaSuccess) return e;
-  k_extend_tc<D, kWin><<<grid, kThreads, smem, s>>>(L.tmk, L.tmv, tmq, tmo, P);
+  k_extend_tc<D, kWin, kF8><<<grid, kF8 ? kThreadsF8 : kThreads, smem, s>>>(L.tmk, L.tmv, tmq, tmo, P);
   return cudaGetLastError();
 }
 
 bool tc_extend_supported(const Ctx &c, int layer) {
-  if (!c.layers[layer].tma || c.cfg.kv_dtype != SWA_DTYPE_BF16 ||
-      (c.cfg.head_dim != 64 && c.cfg.head_dim != 128) || c.cfg.page_size > 64)
+  const bool f8 = c.cfg.kv_dtype == SWA_DTYPE_E4M3;
+  if (!c.layers[layer].tma || (c.cfg.kv_dtype != SWA_DTYPE_BF16 && !f8) ||
+      (c.cfg.head_dim != 64 && c.cfg.head_dim != 128) || (f8 && c.cfg.head_dim != 128) ||
+      c.cfg.page_size > 64)
     return false;
   const int G = c.cfg.num_q_heads / c.layers[layer].hkv;
   return G >= 1 && G <= kRows;
@@ -991,6 +1180,12 @@ cudaError_t launch_attn_extend_tc(Ctx &c, const AttnArgs &a, cudaStream_t s) {
   P.scale_log2 = a.scale * 1.4426950408889634f;
   P.out = static_cast<__nv_bfloat16 *>(a.out);
   P.err = c.err_word;
+  const bool f8 = c.cfg.kv_dtype == SWA_DTYPE_E4M3;
+  P.k8 = reinterpret_cast<const uint8_t *>(L.addr.k);
+  P.v8 = reinterpret_cast<const uint8_t *>(L.addr.v);
+  P.row_bytes = L.addr.row_bytes;
+  P.k_scale = a.k_scale;
+  P.v_scale = a.v_scale;
   // Persistent: one CTA per SM (the KV heads share the SMs), each looping
   // over its items.
   const int per_head = std::max(1, (c.num_sms > 0 ? c.num_sms : 148) / L.hkv);
@@ -1002,10 +1197,14 @@ cudaError_t launch_attn_extend_tc(Ctx &c, const AttnArgs &a, cudaStream_t s) {
       !make_qo_tensor_map(&tmo, a.out, a.nq, c.cfg.num_q_heads, c.cfg.head_dim, P.G))
     return cudaErrorInvalidValue;
   const bool win = L.kind != SWA_LAYER_FULL;
+  if (f8)
+    return win ? launch_d<128, true, true>(grid, L, tmq, tmo, P, s)
+               : launch_d<128, false, true>(grid, L, tmq, tmo, P, s);
   if (c.cfg.head_dim == 64)
-    return win ? launch_d<64, true>(grid, L, tmq, tmo, P, s) : launch_d<64, false>(grid, L, tmq, tmo, P, s);
-  return win ? launch_d<128, true>(grid, L, tmq, tmo, P, s)
-             : launch_d<128, false>(grid, L, tmq, tmo, P, s);
+    return win ? launch_d<64, true, false>(grid, L, tmq, tmo, P, s)
+               : launch_d<64, false, false>(grid, L, tmq, tmo, P, s);
+  return win ? launch_d<128, true, false>(grid, L, tmq, tmo, P, s)
+             : launch_d<128, false, false>(grid, L, tmq, tmo, P, s);
 }
 
 }  // namespace swa

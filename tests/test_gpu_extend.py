@@ -19,9 +19,10 @@ LAYERS = [(OT.SLIDING, 127, 8), (OT.FULL, 0, 4)]
 GPTOSS_LAYERS = [(OT.SLIDING, 127, 8), (OT.FULL, 0, 8)]      # G = 8, D = 64
 
 
-def _run(ps, path, prompt, chunk, layers=LAYERS, chunk0=256, D=128, Hq=64):
-    P = Pair(layers, Hq=Hq, D=D, dtype="bf16", ps=ps, size_full=ps * (4096 // ps + 40),
-             size_swa=ps * (1536 // ps + 40), seed=11, perm_free=True, max_ctx=4096, max_reqs=4)
+def _run(ps, path, prompt, chunk, layers=LAYERS, chunk0=256, D=128, Hq=64, dtype="bf16", **kw):
+    P = Pair(layers, Hq=Hq, D=D, dtype=dtype, ps=ps, size_full=ps * (4096 // ps + 40),
+             size_swa=ps * (1536 // ps + 40), seed=11, perm_free=True, max_ctx=4096, max_reqs=4,
+             **kw)
     api.swa_set_attn_path(P.ctx, path)
     rows = [1, 2, 3]
     lens = np.zeros(3, np.int64)
@@ -144,4 +145,24 @@ def test_extend_group_sizes_not_dividing_128(Hq, layers):
     assert api.swa_last_attn_path(P.ctx) == 2
     for l, (g, o) in res.items():
         assert_close(g, o, 2e-2, f"Hq={Hq} layer {l}")
+    assert api.swa_device_check(P.ctx) == 0
+
+
+@pytest.mark.parametrize("layout", ["per_layer", "envelope"])
+@pytest.mark.parametrize("Hq,layers", [
+    pytest.param(40, [(OT.CHUNKED, 192, 8), (OT.SLIDING, 127, 8), (OT.FULL, 0, 8)], id="G5"),
+    pytest.param(64, LAYERS, id="G8-G16"),
+])
+@pytest.mark.parametrize("path,expect", [pytest.param(-1, 2, id="tcgen05"),
+                                         pytest.param(0, 0, id="generic")])
+def test_extend_e4m3(layout, Hq, layers, path, expect):
+    """E4M3 KV (per-layer pools and the page-major envelope, K and V scales
+    0.41 and 1.7): the tensor-core kernel converts K/V to f16 in shared memory
+    and runs f16 products; Llama4-shaped heads (G = 5) with chunked-local,
+    sliding and full layers, and MiMo-shaped ones, against the oracle."""
+    P, res = _run(64, path, prompt=[700, 333, 0], chunk=[150, 77, 40], layers=layers, Hq=Hq,
+                  dtype="e4m3", layout=layout, k_scale=0.41, v_scale=1.7)
+    assert api.swa_last_attn_path(P.ctx) == expect
+    for l, (g, o) in res.items():
+        assert_close(g, o, 2e-2, f"e4m3 {layout} Hq={Hq} layer {l}")
     assert api.swa_device_check(P.ctx) == 0
