@@ -1,13 +1,14 @@
 // Chunked-prefill (extend) attention on the 5th-generation tensor cores
-// (tcgen05 + TMEM + TMA), bf16 KV in the per-layer layout, D = 64 or 128,
-// any GQA group G up to 128, page size 16..64 (a power of two).
+// (tcgen05 + TMEM + TMA): bf16 KV with D = 64 or 128, or E4M3 KV with D = 128
+// (per-layer pools or the page-major envelope), any GQA group G up to 128,
+// page size 16..64 (a power of two).
 //
 // Method: "SWA in SGLang" design note - the chunk's queries at positions
 // pre..seq-1 attend causally; sliding layers see the last Wx+1 keys, full
 // layers every earlier key; a per-head sink joins the denominator.
 //
 // GB300 design (persistent: one CTA per SM loops over work items; 10 warps,
-// warp-specialised; TMEM and barriers set up once per CTA, barrier phases
+// 12 for E4M3 KV, warp-specialised; TMEM and barriers set up once per CTA, barrier phases
 // following running counts, so that no role waits for the others at an item
 // boundary):
 //   * an item is two Q tiles of up to 128 rows, each floor(128/G) consecutive
@@ -32,12 +33,14 @@
 //     every hand-off;
 //   * warps 0-3 and 4-7 are the softmax groups of Q tile 0 and 1: each thread
 //     owns one row (one TMEM lane), reads its S row, masks only the key tiles
-//     that straddle a window or causal edge, and keeps a lazily rescaled
-//     running maximum (O in TMEM is rescaled only when the maximum grew by more
-//     than 2^8), writes P as packed bf16 pairs back to TMEM and signals the
-//     MMA lane; after the item's last tile it normalises O (with the sink) and
-//     stores its output row, while the tensor core already computes the next
-//     item's first S.
+//     (64-key chunks on windowed layers) that straddle a window or causal
+//     edge, and keeps a lazily rescaled running maximum (O in TMEM is rescaled
+//     only when the maximum grew by more than 2^8), writes P as packed bf16
+//     (f16 for E4M3 KV) pairs back to TMEM and signals the MMA lane; after the
+//     item's last tile it normalises O (with the sink) and stores its output
+//     rows, while the tensor core already computes the next item's first S;
+//   * E4M3 KV only: warps 10 and 11 convert the K/V rows and the Q tiles to
+//     f16 (below, at the kernel).
 // KV pools are zero-initialised by the caller (as the pages' pools are), so
 // rows of a loaded page outside the query's key range hold finite values and
 // their zero softmax weight cancels them exactly; page slots of a key tile
@@ -778,7 +781,6 @@ __global__ void __launch_bounds__(kF8 ? kThreadsF8 : kThreads, 1)
       const int64_t k_hi = it.pfirst + it.n_tok - 1;
       const int64_t pg0 = it.kt0 >> P.ps_shift;
       const int n_pg = (int)((k_hi >> P.ps_shift) - pg0 + 1);
-      const int n_slots = it.n_tiles * ppt;
       const bool full_layer = P.kind == SWA_LAYER_FULL;
       const int32_t *rt_row = full_layer ? P.rt + P.req_idx[it.b] * P.rt_stride : nullptr;
       const int32_t *pages = full_layer ? nullptr : P.plan.pages + (int64_t)it.b * P.plan.max_pages;
@@ -854,7 +856,6 @@ __global__ void __launch_bounds__(kF8 ? kThreadsF8 : kThreads, 1)
         if (t + 1 < it.n_tiles) load_tile(t + 1, 0, w);
         if (t == 0) ok = convert_q(u0 + 1);
       }
-      (void)n_slots;
       tg += it.n_tiles;
       ++nd;
     }
