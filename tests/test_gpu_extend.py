@@ -148,19 +148,26 @@ def test_extend_group_sizes_not_dividing_128(Hq, layers):
     assert api.swa_device_check(P.ctx) == 0
 
 
-@pytest.mark.parametrize("layout", ["per_layer", "envelope"])
-@pytest.mark.parametrize("Hq,layers", [
-    pytest.param(40, [(OT.CHUNKED, 192, 8), (OT.SLIDING, 127, 8), (OT.FULL, 0, 8)], id="G5"),
-    pytest.param(64, LAYERS, id="G8-G16"),
+G5_E4M3 = (40, [(OT.CHUNKED, 192, 8), (OT.SLIDING, 127, 8), (OT.FULL, 0, 8)])
+G8_E4M3 = (64, LAYERS)
+
+
+@pytest.mark.parametrize("shape,layout,ps,path,expect", [
+    pytest.param(G5_E4M3, "envelope", 64, -1, 2, id="G5-envelope-ps64-tcgen05"),
+    pytest.param(G5_E4M3, "per_layer", 16, -1, 2, id="G5-per_layer-ps16-tcgen05"),
+    pytest.param(G5_E4M3, "envelope", 64, 0, 0, id="G5-envelope-ps64-generic"),
+    pytest.param(G8_E4M3, "per_layer", 64, -1, 2, id="G8-G16-per_layer-ps64-tcgen05"),
+    pytest.param(G8_E4M3, "envelope", 16, -1, 2, id="G8-G16-envelope-ps16-tcgen05"),
+    pytest.param(G8_E4M3, "per_layer", 64, 0, 0, id="G8-G16-per_layer-ps64-generic"),
 ])
-@pytest.mark.parametrize("path,expect", [pytest.param(-1, 2, id="tcgen05"),
-                                         pytest.param(0, 0, id="generic")])
-def test_extend_e4m3(layout, Hq, layers, path, expect):
+def test_extend_e4m3(shape, layout, ps, path, expect):
     """E4M3 KV (per-layer pools and the page-major envelope, K and V scales
     0.41 and 1.7): the tensor-core kernel converts K/V to f16 in shared memory
     and runs f16 products; Llama4-shaped heads (G = 5) with chunked-local,
-    sliding and full layers, and MiMo-shaped ones, against the oracle."""
-    P, res = _run(64, path, prompt=[700, 333, 0], chunk=[150, 77, 40], layers=layers, Hq=Hq,
+    sliding and full layers, and MiMo-shaped ones, pages of 64 and 16 (a key
+    tile over 2 or 8 pages), against the oracle."""
+    Hq, layers = shape
+    P, res = _run(ps, path, prompt=[700, 333, 0], chunk=[150, 77, 40], layers=layers, Hq=Hq,
                   dtype="e4m3", layout=layout, k_scale=0.41, v_scale=1.7)
     assert api.swa_last_attn_path(P.ctx) == expect
     for l, (g, o) in res.items():
