@@ -701,6 +701,8 @@ swa_status swa_attn_extend(swa_ctx *c, int32_t layer, int32_t bs, const int32_t 
   if (!prefix_lens || !seq_lens || !qo_indptr || !q || !out || max_new < 1 || max_seq_len < 1 ||
       (L.in_full && (!rt || !req_idx)) || (!L.in_full && !plan))
     return fail(c, SWA_ERR_INVALID, "bad attention args");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15)
+    return fail(c, SWA_ERR_INVALID, "q and out must be 16-byte aligned");
   if (ws_bytes < swa_attn_extend_ws_bytes(c, layer, n_tokens, max_seq_len) || !ws)
     return fail(c, SWA_ERR_INVALID, "split workspace too small");
   const bool tc = use_tc(c, layer);

@@ -594,7 +594,13 @@ swa_status swa_attn_decode_noalloc(swa_ctx *ctx, int32_t layer, int32_t bs,
 /* swa_attn_extend: chunked-prefill queries.  Request b owns query rows
  * qo_indptr[b]..qo_indptr[b+1]-1 (device, bs+1 entries), at positions
  * prefix_lens[b] .. seq_lens[b]-1, causal.  n_tokens = qo_indptr[bs] and
- * max_new >= max(seq - prefix) are host values. */
+ * max_new >= max(seq - prefix) are host values.  q and out are device
+ * [n_tokens][num_q_heads][head_dim] arrays (f32 for an F32 pool, bf16
+ * otherwise), both 16-byte aligned (SWA_ERR_INVALID otherwise).  The tcgen05
+ * kernel serves bf16 pools with head_dim 64 or 128 and E4M3 pools with
+ * head_dim 128, any query-per-KV-head group up to 128 and page sizes 16..64;
+ * other configurations run the generic kernel, which takes at most 65535
+ * tokens per call. */
 size_t swa_attn_extend_ws_bytes(const swa_ctx *ctx, int32_t layer,
                                 int64_t n_tokens, int32_t max_seq_len);
 swa_status swa_attn_extend(swa_ctx *ctx, int32_t layer, int32_t bs,
