@@ -80,6 +80,7 @@ struct Geo {
 constexpr uint32_t kTmemCols = 512;
 constexpr long kSpinLimit = 1L << 24;
 constexpr float kRescaleGap = 8.f;           // log2 units: rescale O when the max grows more
+constexpr float kSumCap = 65536.f;           // a chunk's weight sum that forces a maximum pass
 
 struct TcParams {
   int kind, window, hkv, G, ps, ps_shift;
@@ -940,68 +941,90 @@ __global__ void __launch_bounds__(kF8 ? kThreadsF8 : kThreads, 1)
           tc_wait_ld();
           if (kWin ? __any_sync(0xffffffffu, e_lo > c0 || e_hi < c0 + 63) : masked)
             mask_in_place(rr, cb);
-          // four independent chains of three-input maxima
-          float m2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-  #pragma unroll
-          for (int e = 0; e < 64; e += 2)
-            m2[(e >> 1) & 3] = max3(m2[(e >> 1) & 3], __uint_as_float(rr[e]), __uint_as_float(rr[e + 1]));
-          float cm = max3(m2[0], m2[1], fmaxf(m2[2], m2[3]));
-          cm = cm == -INFINITY ? -INFINITY : cm * sc;
-          // A row whose maximum is still -inf has accumulated exactly nothing
-          // (every P so far was 0), so its first finite maximum needs no
-          // rescale (factor 1): only moves of a finite maximum pay for one.
-          float corr = 1.f;
-          if (cm > m_run + kRescaleGap || (m_run == -INFINITY && cm != -INFINITY)) {
-            corr = m_run == -INFINITY ? 1.f : exp2f(m_run - cm);
-            m_run = cm;
-          }
-          if (__any_sync(0xffffffffu, corr != 1.f)) {
-            if (t > 0) {
-  #pragma unroll 1
-              for (int ob = 0; ob < kD / 32; ++ob) {
-                uint32_t ro[32];
-                TC_LD32(tO + ob * 32, ro);
-                tc_wait_ld();
-  #pragma unroll
-                for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * corr);
-                TC_ST32(tO + ob * 32, ro);
-              }
-            }
-            if (cb == 1) {
-              // the first chunk's P (32 columns of bf16 pairs) against the new reference
-              uint32_t pp[32];
-              tc_wait_st();
-              TC_LD32(tS, pp);
-              tc_wait_ld();
-  #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const float2 f = unpack_p<kF8>(pp[e]);
-                pp[e] = pack_p<kF8>(f.x * corr, f.y * corr);
-              }
-              TC_ST32(tS, pp);
-            }
-            float a0, a1, b0, b1;
-            f2unpack(acc2[0], a0, a1);
-            f2unpack(acc2[1], b0, b1);
-            acc2[0] = f2pack(a0 * corr, a1 * corr);
-            acc2[1] = f2pack(b0 * corr, b1 * corr);
-            l_run *= corr;
-          }
-          const float mu = m_run == -INFINITY ? 0.f : m_run;
-          const uint64_t nmu2 = f2pack(-mu, -mu);
-          // P = exp2(scale*s - m) as packed bf16 pairs, written over the S
-          // columns already consumed (64-key chunk cb -> columns [32 cb, 32 cb + 32)).
+          // The reference maximum m_run moves only when needed: for a row's
+          // first chunk (no reference yet), or when the chunk's weights against
+          // the current reference sum past kSumCap (some score outgrew the
+          // reference by more than log2 kSumCap - 6); otherwise the chunk's
+          // maximum is never computed.  A chunk whose sum overflowed is
+          // recomputed once against the raised reference.
+          bool redo = __any_sync(0xffffffffu, m_run == -INFINITY);
           uint32_t pk[32];
+          uint64_t c2[2];   // this chunk's pair sums
+  #pragma unroll 1
+          for (int pass = 0;; ++pass) {
+            if (redo) {
+              // four independent chains of three-input maxima
+              float m2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
   #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float t0, t1;
-            f2unpack(fma2(f2pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1])), sc2, nmu2),
-                     t0, t1);
-            const float a0 = ex2(t0);
-            const float a1 = ex2(t1);
-            acc2[e & 1] = add2(acc2[e & 1], f2pack(a0, a1));
-            pk[e] = pack_p<kF8>(a0, a1);
+              for (int e = 0; e < 64; e += 2)
+                m2[(e >> 1) & 3] = max3(m2[(e >> 1) & 3], __uint_as_float(rr[e]), __uint_as_float(rr[e + 1]));
+              float cm = max3(m2[0], m2[1], fmaxf(m2[2], m2[3]));
+              cm = cm == -INFINITY ? -INFINITY : cm * sc;
+              // A row whose maximum is still -inf has accumulated exactly nothing
+              // (every P so far was 0), so its first finite maximum needs no
+              // rescale (factor 1): only moves of a finite maximum pay for one.
+              float corr = 1.f;
+              if (cm > m_run + kRescaleGap || (m_run == -INFINITY && cm != -INFINITY)) {
+                corr = m_run == -INFINITY ? 1.f : exp2f(m_run - cm);
+                m_run = cm;
+              }
+              if (__any_sync(0xffffffffu, corr != 1.f)) {
+                if (t > 0) {
+  #pragma unroll 1
+                  for (int ob = 0; ob < kD / 32; ++ob) {
+                    uint32_t ro[32];
+                    TC_LD32(tO + ob * 32, ro);
+                    tc_wait_ld();
+  #pragma unroll
+                    for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * corr);
+                    TC_ST32(tO + ob * 32, ro);
+                  }
+                }
+                if (cb == 1) {
+                  // the first chunk's P (32 columns of bf16 pairs) against the new reference
+                  uint32_t pp[32];
+                  tc_wait_st();
+                  TC_LD32(tS, pp);
+                  tc_wait_ld();
+  #pragma unroll
+                  for (int e = 0; e < 32; ++e) {
+                    const float2 f = unpack_p<kF8>(pp[e]);
+                    pp[e] = pack_p<kF8>(f.x * corr, f.y * corr);
+                  }
+                  TC_ST32(tS, pp);
+                }
+                float a0, a1, b0, b1;
+                f2unpack(acc2[0], a0, a1);
+                f2unpack(acc2[1], b0, b1);
+                acc2[0] = f2pack(a0 * corr, a1 * corr);
+                acc2[1] = f2pack(b0 * corr, b1 * corr);
+                l_run *= corr;
+              }
+            }
+            const float mu = m_run == -INFINITY ? 0.f : m_run;
+            const uint64_t nmu2 = f2pack(-mu, -mu);
+            // P = exp2(scale*s - m) as packed bf16 pairs, written over the S
+            // columns already consumed (64-key chunk cb -> columns [32 cb, 32 cb + 32)).
+            c2[0] = c2[1] = 0ull;
+  #pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              float t0, t1;
+              f2unpack(fma2(f2pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1])), sc2, nmu2),
+                       t0, t1);
+              const float a0 = ex2(t0);
+              const float a1 = ex2(t1);
+              c2[e & 1] = add2(c2[e & 1], f2pack(a0, a1));
+              pk[e] = pack_p<kF8>(a0, a1);
+            }
+            if (pass == 1) break;
+            float s0, s1, s2, s3;
+            f2unpack(c2[0], s0, s1);
+            f2unpack(c2[1], s2, s3);
+            redo = __any_sync(0xffffffffu, (s0 + s1) + (s2 + s3) > kSumCap);
+            if (!redo) break;
           }
+          acc2[0] = add2(acc2[0], c2[0]);
+          acc2[1] = add2(acc2[1], c2[1]);
           TC_ST32(tS + cb * 32, pk);
         }
         {

@@ -173,3 +173,30 @@ def test_extend_e4m3(shape, layout, ps, path, expect):
     for l, (g, o) in res.items():
         assert_close(g, o, 2e-2, f"e4m3 {layout} Hq={Hq} layer {l}")
     assert api.swa_device_check(P.ctx) == 0
+
+
+def test_extend_rejects_misaligned_queries():
+    """q or out not 16-byte aligned (the tensor-core kernel moves them by TMA):
+    SWA_ERR_INVALID before anything is launched, and the context stays usable."""
+    P = Pair(LAYERS, Hq=64, D=128, dtype="bf16", ps=64, size_full=64 * 80, size_swa=64 * 40,
+             seed=3, max_ctx=1024, max_reqs=2)
+    rows, pre, seq = [1], np.array([0]), np.array([40])
+    P.extend(rows, pre, seq)
+    d = lambda x: torch.tensor(np.asarray(x, np.int64), device="cuda")
+    plan = torch.zeros(api.swa_plan_bytes(P.ctx, 1, 40), dtype=torch.uint8, device="cuda")
+    api.swa_plan(P.ctx, P.rt, d(rows), d(pre), d(seq), plan, 40)
+    ws = torch.zeros(api.swa_attn_extend_ws_bytes(P.ctx, 1, 40, 40), dtype=torch.uint8,
+                     device="cuda")
+    buf = torch.zeros(40 * 64 * 128 + 8, dtype=torch.bfloat16, device="cuda")
+    good = buf[:40 * 64 * 128].view(40, 64, 128)
+    bad = buf[1:1 + 40 * 64 * 128].view(40, 64, 128)      # 2 bytes off
+    out = torch.empty_like(good)
+    for q, o in ((bad, out), (good, bad)):
+        with pytest.raises(api.SwaError) as e:
+            api.swa_attn_extend(P.ctx, 1, P.rt, d(rows), d(pre), d(seq), d([0, 40]), 40, 40, 40,
+                                plan, q, P.sinks_d[1], P.scale, o, ws)
+        assert e.value.status == api.SWA_ERR_INVALID
+    api.swa_attn_extend(P.ctx, 1, P.rt, d(rows), d(pre), d(seq), d([0, 40]), 40, 40, 40, plan,
+                        good, P.sinks_d[1], P.scale, out, ws)
+    torch.cuda.synchronize()
+    assert api.swa_device_check(P.ctx) == 0
