@@ -17,10 +17,11 @@ running one is never reached.  These cases reach it:
   far above the scores.
 
 The extend cases prove that the tensor-core kernel's lazy rescale fired: a CPU
-model of its block loop (64-key blocks, reference maximum moved only when a
-block exceeds it by more than 8 log2 units) counts rescale events on the
-first and on the second block of a 128-key tile over the same inputs, and the
-same model with the rescale left out misses the oracle by more than the
+model of its block loop (64-key blocks; a block's maximum computed only when
+its weights against the reference sum past 2^16, the reference moved when
+that maximum exceeds it by more than 8 log2 units) counts rescale events on
+the first and on the second block of a 128-key tile over the same inputs, and
+the same model with the rescale left out misses the oracle by more than the
 tolerance - so a kernel that skipped it would fail here."""
 import numpy as np
 import pytest
@@ -73,16 +74,21 @@ def _build(P, rows, prompt, chunk0=512):
 # ---------------------------------------------------------------------------
 def lazy_block_softmax(s2, keys, V, sink2, skip_rescale=False):
     """Output of one row by the kernel's loop: 64-key blocks at 64-aligned
-    key positions, a reference maximum moved only when a block's maximum
-    exceeds it by more than 8 (log2 units), weights 2^(s - m).  Returns
-    (output, rescale events on block parity 0, events on parity 1)."""
+    key positions; a block's weights 2^(s - m) are taken against the current
+    reference maximum m, and only when there is no reference yet or they sum
+    past 2^16 is the block's maximum computed, m moving when that maximum
+    exceeds it by more than 8 (log2 units).  Returns (output, rescale events
+    on block parity 0, events on parity 1)."""
     m, l = -np.inf, 0.0
     o = np.zeros(V.shape[1])
     ev = [0, 0]
     blocks = keys // 64
     for blk in np.unique(blocks):
         sel = blocks == blk
-        cm = s2[sel].max()
+        if m != -np.inf and (2.0 ** (s2[sel] - m)).sum() <= 65536.0:
+            cm = -np.inf      # no maximum pass: the reference stays
+        else:
+            cm = s2[sel].max()
         if cm > m + 8 or (m == -np.inf and cm != -np.inf):
             if m != -np.inf:
                 ev[int(blk) & 1] += 1
